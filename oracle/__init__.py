@@ -1,0 +1,128 @@
+"""Plain fp64 CPU oracle for the block-quantized weight x activation product.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product library
+never calls it and shares no code with it.
+
+The arithmetic lives in ``lean_oracle.c`` (scalar C, fp64): every weight is
+decoded from its canonical block bytes and the dot product is summed in fp64.
+This module only compiles that file with gcc and marshals numpy arrays to it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lean_oracle.c")
+_LIB = os.path.join(_HERE, "liblean_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+Q4_0, Q8_0, I8_B64, Q6_K = 0, 1, 2, 3
+
+
+def build(force: bool = False) -> str:
+    """Compile lean_oracle.c into liblean_oracle.so next to it (gcc, -O2)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".tmp.%d" % os.getpid()
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                    "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            c_i64, c_int = ctypes.c_int64, ctypes.c_int
+            vp = ctypes.c_void_p
+            lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_fp16_to_double.restype = ctypes.c_double
+            lib.oracle_block_elems.argtypes = [c_int]
+            lib.oracle_block_elems.restype = c_int
+            lib.oracle_block_bytes.argtypes = [c_int]
+            lib.oracle_block_bytes.restype = c_int
+            lib.oracle_dequant.argtypes = [c_int, vp, c_i64, c_i64, vp]
+            lib.oracle_dequant.restype = c_int
+            lib.oracle_qmatmul.argtypes = [c_int, vp, vp, vp, vp, c_i64, c_i64, c_i64, c_int]
+            lib.oracle_qmatmul.restype = c_int
+            lib.oracle_qmatmul_pairs.argtypes = [c_int, vp, vp, c_i64, c_i64, c_i64, c_i64,
+                                                 vp, vp, vp, vp]
+            lib.oracle_qmatmul_pairs.restype = c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def fp16_to_double(bits: int) -> float:
+    return _load().oracle_fp16_to_double(bits)
+
+
+def block_elems(fmt: int) -> int:
+    return _load().oracle_block_elems(fmt)
+
+
+def block_bytes(fmt: int) -> int:
+    return _load().oracle_block_bytes(fmt)
+
+
+def _check_w(fmt, W, N, K):
+    be, bb = block_elems(fmt), block_bytes(fmt)
+    if be == 0 or K % be:
+        raise ValueError("bad format or K")
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    if W.size != N * (K // be) * bb:
+        raise ValueError("W has %d bytes, expected %d" % (W.size, N * (K // be) * bb))
+    return W
+
+
+def dequant(fmt: int, W: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Exact fp64 weights w[N][K] decoded from canonical blocks."""
+    W = _check_w(fmt, W, N, K)
+    w = np.empty((N, K), dtype=np.float64)
+    if _load().oracle_dequant(fmt, _ptr(W), N, K, _ptr(w)):
+        raise ValueError("oracle_dequant failed")
+    return w
+
+
+def qmatmul(fmt: int, W: np.ndarray, x: np.ndarray, N: int, K: int,
+            threads: int = 1):
+    """Return (y[M][N], bound[M][N]) in fp64 for canonical W and fp32 x[M][K]."""
+    W = _check_w(fmt, W, N, K)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, K)
+    M = x.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    b = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_qmatmul(fmt, _ptr(W), _ptr(x), _ptr(y), _ptr(b), N, K, M, threads)
+    if rc:
+        raise ValueError("oracle_qmatmul failed (%d)" % rc)
+    return y, b
+
+
+def qmatmul_pairs(fmt: int, W: np.ndarray, x: np.ndarray, N: int, K: int,
+                  m_idx, n_idx):
+    """(y, bound) for the selected output pairs (m_idx[i], n_idx[i]) only."""
+    W = _check_w(fmt, W, N, K)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, K)
+    m_idx = np.ascontiguousarray(m_idx, dtype=np.int64)
+    n_idx = np.ascontiguousarray(n_idx, dtype=np.int64)
+    P = m_idx.size
+    y = np.empty(P, dtype=np.float64)
+    b = np.empty(P, dtype=np.float64)
+    rc = _load().oracle_qmatmul_pairs(fmt, _ptr(W), _ptr(x), N, K, x.shape[0], P,
+                                      _ptr(m_idx), _ptr(n_idx), _ptr(y), _ptr(b))
+    if rc:
+        raise ValueError("oracle_qmatmul_pairs failed (%d)" % rc)
+    return y, b
