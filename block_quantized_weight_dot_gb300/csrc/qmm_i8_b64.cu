@@ -1,0 +1,8 @@
+// qmm_i8_b64.cu -- I8_B64 instantiation of the CUDA-core product and dequant kernels.
+#include "simt_launch.cuh"
+
+namespace lean {
+template lean_status qmm_fmt<I8_B64>(const Geom &, const uint8_t *, const float *, float *, int64_t,
+                                 cudaStream_t);
+template lean_status dequant_fmt<I8_B64>(const Geom &, const uint8_t *, float *, cudaStream_t);
+}  // namespace lean

@@ -1,0 +1,165 @@
+"""ctypes binding of ``liblean_qmatmul.so`` (C ABI in ``include/lean_qmatmul.h``).
+
+Argument marshalling only: every computation of the product runs in the CUDA
+library.  Functions keep the C names.  Buffers may be given as torch tensors
+(their ``data_ptr()`` is passed), numpy arrays (host calls only) or raw integer
+addresses.  A non-OK status raises :class:`LeanError`.  If the library has not
+been built the import fails: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblean_qmatmul.so")
+
+LEAN_Q4_0, LEAN_Q8_0, LEAN_I8_B64, LEAN_Q6_K = 0, 1, 2, 3
+LEAN_OK, LEAN_ERR_FORMAT, LEAN_ERR_SHAPE, LEAN_ERR_NULL, LEAN_ERR_ALIGN, LEAN_ERR_CUDA = range(6)
+
+# every symbol the header declares, with (restype, argtypes)
+_i64, _int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+SIGNATURES = {
+    "lean_block_elems": (_int, [_int]),
+    "lean_block_bytes": (_i64, [_int]),
+    "lean_canonical_bytes": (_i64, [_int, _i64, _i64]),
+    "lean_packed_bytes": (_i64, [_int, _i64, _i64]),
+    "lean_pack": (_int, [_int, _vp, _vp, _i64, _i64]),
+    "lean_unpack_canonical": (_int, [_int, _vp, _vp, _i64, _i64]),
+    "lean_dequant": (_int, [_int, _vp, _vp, _i64, _i64, _vp]),
+    "lean_qmatmul": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "lean_status_str": (ctypes.c_char_p, [_int]),
+}
+
+
+class LeanError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (fn, status_str(status), status))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("liblean_qmatmul.so is not built: run "
+                          "`python -c \"import __graft_entry__ as g; g.build()\"`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _addr(buf):
+    """Address of a buffer: torch tensor, numpy array, int or None."""
+    if buf is None:
+        return None
+    if isinstance(buf, int):
+        return buf
+    if isinstance(buf, np.ndarray):
+        return buf.ctypes.data
+    if hasattr(buf, "data_ptr"):
+        return buf.data_ptr()
+    raise TypeError("unsupported buffer type %r" % type(buf))
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream  # torch.cuda.Stream
+
+
+def _check(fn, status):
+    if status != LEAN_OK:
+        raise LeanError(fn, status)
+
+
+def status_str(status: int) -> str:
+    return _lib.lean_status_str(status).decode()
+
+
+lean_status_str = status_str
+
+
+def lean_block_elems(fmt: int) -> int:
+    return _lib.lean_block_elems(fmt)
+
+
+def lean_block_bytes(fmt: int) -> int:
+    return _lib.lean_block_bytes(fmt)
+
+
+def lean_canonical_bytes(fmt: int, N: int, K: int) -> int:
+    return _lib.lean_canonical_bytes(fmt, N, K)
+
+
+def lean_packed_bytes(fmt: int, N: int, K: int) -> int:
+    return _lib.lean_packed_bytes(fmt, N, K)
+
+
+def lean_pack(fmt: int, canon, N: int, K: int, packed=None) -> np.ndarray:
+    """Canonical host bytes -> packed host bytes (a new uint8 array unless given)."""
+    canon = np.ascontiguousarray(canon, dtype=np.uint8)
+    nb = lean_packed_bytes(fmt, N, K)
+    if nb < 0:
+        raise LeanError("lean_pack", LEAN_ERR_SHAPE)
+    if canon.size != lean_canonical_bytes(fmt, N, K):
+        raise ValueError("canonical buffer has %d bytes, expected %d"
+                         % (canon.size, lean_canonical_bytes(fmt, N, K)))
+    if packed is None:
+        packed = np.empty(nb, dtype=np.uint8)
+    _check("lean_pack", _lib.lean_pack(fmt, _addr(canon), _addr(packed), N, K))
+    return packed
+
+
+def lean_unpack_canonical(fmt: int, packed, N: int, K: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    if packed.size != lean_packed_bytes(fmt, N, K):
+        raise ValueError("packed buffer has the wrong size")
+    canon = np.empty(lean_canonical_bytes(fmt, N, K), dtype=np.uint8)
+    _check("lean_unpack_canonical", _lib.lean_unpack_canonical(fmt, _addr(packed), _addr(canon), N, K))
+    return canon
+
+
+def lean_dequant(fmt: int, W_packed_dev, w_dev, N: int, K: int, stream=None) -> None:
+    _check("lean_dequant", _lib.lean_dequant(fmt, _addr(W_packed_dev), _addr(w_dev), N, K,
+                                             _stream(stream)))
+
+
+def lean_qmatmul(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,
+                 stream=None) -> None:
+    """y[M][N] = x[M][K] . W[N][K]^T on the device, asynchronously on `stream`."""
+    _check("lean_qmatmul", _lib.lean_qmatmul(fmt, _addr(W_packed_dev), _addr(x_dev),
+                                             _addr(y_dev), N, K, M, _stream(stream)))
+
+
+# ---- torch conveniences (device memory via PyTorch; compute via the library) ----
+
+def upload_packed(fmt: int, canon, N: int, K: int, device="cuda"):
+    """Pack canonical host bytes and copy them to a new uint8 device tensor."""
+    import torch
+    packed = lean_pack(fmt, canon, N, K)
+    return torch.from_numpy(packed).to(device)
+
+
+def qmatmul(fmt: int, W_packed_dev, x, N: int, K: int, out=None, stream=None):
+    """Allocate y (or use `out`) and run lean_qmatmul; x is a [M, K] fp32 cuda tensor."""
+    import torch
+    x = x.contiguous()
+    M = x.numel() // K
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
+    lean_qmatmul(fmt, W_packed_dev, x, y, N, K, M, stream)
+    return y

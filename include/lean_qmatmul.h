@@ -1,0 +1,138 @@
+/*
+ * lean_qmatmul.h -- C ABI of the GB300 (sm_103a) block-quantized weight x
+ * activation product:  y[m][n] = sum_k w[n][k] * x[m][k].
+ *
+ * The operation is the linear layer of the small LLM engines described on the
+ * "lean" README (llm-web), the "wgpu-llm" README and the "oxinfer" crate page:
+ * during single-sequence decode every linear streams its quantized weights
+ * once ("oxinfer" crate page, Performance: decode is memory-bandwidth bound),
+ * so the product reads the packed blocks directly and never materialises
+ * dense weights.
+ *
+ * Weight formats (block along K, within one output row n):
+ *   LEAN_Q4_0    32 weights, fp16 scale d, 4-bit q:      w = d * (q - 8)
+ *                ("oxinfer", How it works: two nibbles per byte, f16 scale;
+ *                 "lean" README model table: Q4_0 weights)
+ *   LEAN_Q8_0    32 weights, fp16 scale d, int8 q:       w = d * q
+ *                ("lean" README: Q8_0 checkpoints; "oxinfer": 32 weights per
+ *                 scale)
+ *   LEAN_I8_B64  64 weights, fp16 scale d, int8 q:       w = d * q
+ *                ("wgpu-llm" README, INT8 mode: symmetric, block size 64)
+ *   LEAN_Q6_K   256 weights, fp16 d, 16 int8 sub-scales sc (one per 16
+ *                weights), 6-bit q:                      w = d * sc * (q - 32)
+ *                ("lean" README model table: Q6_K embedding)
+ *
+ * Two byte layouts exist:
+ *   canonical  the interchange format (GGUF-style blocks, little-endian):
+ *                Q4_0    [d fp16][16 B: element j<16 = low nibble of byte j,
+ *                                  element j+16 = high nibble of byte j]
+ *                Q8_0    [d fp16][32 x int8]
+ *                I8_B64  [d fp16][64 x int8]
+ *                Q6_K    [ql 128 B][qh 64 B][sc 16 x int8][d fp16]; element e:
+ *                        h = e/128, g = (e%128)/32, l = e%32; low 4 bits =
+ *                        nibble g/2 of ql[64h + 32(g%2) + l], high 2 bits =
+ *                        bits 2g..2g+1 of qh[32h + l], sub-scale sc[e/16]
+ *              A row is K / block_elems consecutive blocks; the matrix is N
+ *              consecutive rows.
+ *   packed     the device layout the kernels stream: a quant plane and a
+ *              scale plane, as the "oxinfer" crate page keeps each quantized
+ *              matrix as quant bytes plus scales "in exactly the in-memory
+ *              layout of the kernels" (Pre-quantized checkpoints).  Rows are
+ *              grouped by 32 and interleaved in 16-byte chunks so that one
+ *              warp's load is 512 contiguous bytes.  Its size is
+ *              lean_packed_bytes(); its contents are private to this library
+ *              and made only by lean_pack().
+ *
+ * Conventions for every call:
+ *   - fmt is one of the lean_fmt values (passed as int).
+ *   - N, K, M > 0; K must be a multiple of lean_block_elems(fmt).
+ *   - The caller owns and allocates every buffer.  Device pointers must come
+ *     from the current CUDA device.  The library never allocates, frees or
+ *     synchronises, and keeps no per-call state.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t passed as
+ *     void*, NULL = the legacy default stream) and make no host read-back, so
+ *     they may be captured into a CUDA graph.
+ *   - Argument errors are detected on the host and returned before any launch.
+ *     A failed launch returns LEAN_ERR_CUDA (cudaGetLastError is consumed).
+ */
+#ifndef LEAN_QMATMUL_H
+#define LEAN_QMATMUL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LEAN_Q4_0 = 0,
+    LEAN_Q8_0 = 1,
+    LEAN_I8_B64 = 2,
+    LEAN_Q6_K = 3
+} lean_fmt;
+
+typedef enum {
+    LEAN_OK = 0,
+    LEAN_ERR_FORMAT = 1, /* unknown fmt                                     */
+    LEAN_ERR_SHAPE = 2,  /* N, K or M <= 0, K not a multiple of the block,
+                            or a size beyond the library's limits           */
+    LEAN_ERR_NULL = 3,   /* a required pointer is NULL                      */
+    LEAN_ERR_ALIGN = 4,  /* a pointer is not aligned as documented          */
+    LEAN_ERR_CUDA = 5    /* the CUDA runtime reported an error              */
+} lean_status;
+
+/* Weights per block: 32, 32, 64, 256.  0 for an unknown fmt. */
+int lean_block_elems(int fmt);
+
+/* Canonical bytes per block: 18, 34, 66, 210.  0 for an unknown fmt. */
+int64_t lean_block_bytes(int fmt);
+
+/* Canonical bytes of an N x K matrix, or -1 on a bad fmt or shape. */
+int64_t lean_canonical_bytes(int fmt, int64_t N, int64_t K);
+
+/* Packed (device layout) bytes of an N x K matrix, or -1 on a bad fmt or
+ * shape.  Rows are padded up to a multiple of 32 and the scale plane to whole
+ * 16-byte vectors, so this is a little more than lean_canonical_bytes(). */
+int64_t lean_packed_bytes(int fmt, int64_t N, int64_t K);
+
+/* Host-side repacking, canonical -> packed.  canon_host holds
+ * lean_canonical_bytes(fmt,N,K) bytes; packed_host receives
+ * lean_packed_bytes(fmt,N,K) bytes (padding is written as zeros).  Both are
+ * host pointers with no alignment requirement.  Blocks are moved bit for bit:
+ * no value is rounded.  Copy the result to the device with cudaMemcpy. */
+lean_status lean_pack(int fmt, const void *canon_host, void *packed_host,
+                      int64_t N, int64_t K);
+
+/* Host-side inverse of lean_pack: packed -> canonical, byte for byte. */
+lean_status lean_unpack_canonical(int fmt, const void *packed_host, void *canon_host,
+                                  int64_t N, int64_t K);
+
+/* Device dequantisation: w_dev[n*K + k] = w[n][k] as fp32 (exact: every
+ * weight of these formats is an fp32 value).  W_packed_dev: 16-byte aligned
+ * device pointer to lean_packed_bytes() bytes made by lean_pack.  w_dev:
+ * 16-byte aligned device buffer of N*K floats, overwritten. */
+lean_status lean_dequant(int fmt, const void *W_packed_dev, float *w_dev,
+                         int64_t N, int64_t K, void *stream);
+
+/* The product.  y[m][n] = sum_k w[n][k] * x[m][k], accumulated in fp32.
+ *   W_packed_dev  device, 16-byte aligned, lean_packed_bytes(fmt,N,K) bytes
+ *                 made by lean_pack (read only)
+ *   x_dev         device, 16-byte aligned, x[M][K] fp32 row-major (read only)
+ *   y_dev         device, 4-byte aligned, y[M][N] fp32 row-major, overwritten
+ *   stream        cudaStream_t as void*
+ * M = 1 is the decode GEMV; small M runs on the CUDA cores with each decoded
+ * weight reused M times; larger M on Q4_0 uses the tcgen05 tensor cores on
+ * split-bf16 operands.  Accuracy: |y - y_exact| <= 1e-4 * sum_k |w x| + 1e-6
+ * per element. */
+lean_status lean_qmatmul(int fmt, const void *W_packed_dev, const float *x_dev,
+                         float *y_dev, int64_t N, int64_t K, int64_t M, void *stream);
+
+/* Static description of a status code. */
+const char *lean_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LEAN_QMATMUL_H */

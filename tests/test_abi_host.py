@@ -1,0 +1,90 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports
+every function include/lean_qmatmul.h declares, and its host calls (sizes,
+packing) behave as documented."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from block_quantized_weight_dot_gb300 import build as lib_build
+from block_quantized_weight_dot_gb300 import synthetic as syn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lean():
+    lib_build.build()
+    from block_quantized_weight_dot_gb300 import lean as L
+    return L
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(lean_\w+)\s*\(", text, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lean):
+    names = declared_functions()
+    assert "lean_qmatmul" in names and "lean_pack" in names
+    lib = ctypes.CDLL(lean.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(lean.SIGNATURES), "binding and header disagree"
+
+
+def test_sizes(lean):
+    for fmt in range(4):
+        assert lean.lean_block_elems(fmt) == syn.BLOCK_ELEMS[fmt]
+        assert lean.lean_block_bytes(fmt) == syn.BLOCK_BYTES[fmt]
+        be = syn.BLOCK_ELEMS[fmt]
+        assert lean.lean_canonical_bytes(fmt, 7, 3 * be) == syn.canonical_bytes(fmt, 7, 3 * be)
+        assert lean.lean_packed_bytes(fmt, 7, 3 * be) >= syn.canonical_bytes(fmt, 7, 3 * be)
+        assert lean.lean_packed_bytes(fmt, 7, be + 1) == -1
+        assert lean.lean_packed_bytes(fmt, 0, be) == -1
+    assert lean.lean_block_elems(9) == 0
+    # Q4_0 960x960: 30 groups x 30 vectors x 512 B + 30 groups x 4 scale vectors x 512 B
+    assert lean.lean_packed_bytes(0, 960, 960) == 30 * 30 * 512 + 30 * 4 * 512
+
+
+@pytest.mark.parametrize("fmt", range(4), ids=[syn.FORMAT_NAMES[f] for f in range(4)])
+def test_pack_round_trip(lean, fmt):
+    be = syn.BLOCK_ELEMS[fmt]
+    for N, K in ((1, be), (33, 3 * be), (70, 11 * be), (31, 17 * be)):
+        W, _ = syn.make_problem(fmt, N, K, 1, seed=(1, fmt, N))
+        p = lean.lean_pack(fmt, W, N, K)
+        assert lean.lean_unpack_canonical(fmt, p, N, K).tobytes() == W.tobytes()
+    # edge blocks: all-zero, all-ones bytes
+    for fill in (0x00, 0xFF, 0x80, 0x7F):
+        W = np.full(syn.canonical_bytes(fmt, 3, 2 * be), fill, np.uint8)
+        p = lean.lean_pack(fmt, W, 3, 2 * be)
+        assert lean.lean_unpack_canonical(fmt, p, 3, 2 * be).tobytes() == W.tobytes()
+
+
+def test_pack_padding_is_zero(lean):
+    """Rows past N in the last 32-row group are written as zeros."""
+    fmt, N, K = 0, 33, 64
+    W = np.full(syn.canonical_bytes(fmt, N, K), 0xFF, np.uint8)
+    p = lean.lean_pack(fmt, W, N, K).reshape(-1)
+    # quant plane: group 1 holds row 32 only -> lanes 1..31 of its vectors are zero
+    q = p[:2 * 2 * 512].reshape(2, 2, 32, 16)
+    assert (q[1, :, 1:, :] == 0).all() and (q[1, :, 0, :] == 0xFF).all()
+
+
+def test_host_argument_errors(lean):
+    f = lean._lib.lean_pack
+    buf = np.zeros(1024, np.uint8)
+    assert f(5, buf.ctypes.data, buf.ctypes.data, 1, 32) == lean.LEAN_ERR_FORMAT
+    assert f(0, None, buf.ctypes.data, 1, 32) == lean.LEAN_ERR_NULL
+    assert f(0, buf.ctypes.data, buf.ctypes.data, 1, 33) == lean.LEAN_ERR_SHAPE
+    for s in range(6):
+        assert lean.status_str(s)

@@ -1,0 +1,140 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Bar: unpacked weights bit-exact; one-hot products bit-exact; every output
+within |y - y_ref| <= 1e-4 * sum_k |w x| + 1e-6.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from block_quantized_weight_dot_gb300 import synthetic as syn
+from lean_testlib import check_close, run_gpu, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [syn.Q4_0, syn.Q8_0, syn.I8_B64, syn.Q6_K]
+IDS = [syn.FORMAT_NAMES[f] for f in FMTS]
+
+
+@pytest.fixture(scope="module")
+def lean():
+    torch_cuda()
+    from block_quantized_weight_dot_gb300 import lean as L
+    return L
+
+
+# ---- unpacked values: bit-exact ------------------------------------------------
+
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+def test_dequant_bit_exact(lean, fmt):
+    torch = torch_cuda()
+    be = syn.BLOCK_ELEMS[fmt]
+    for N, K in ((1, be), (33, 3 * be), (70, 11 * be), (64, 40 * be)):
+        W, _ = syn.make_problem(fmt, N, K, 1, seed=(20, fmt, N, K))
+        Wd = lean.upload_packed(fmt, W, N, K)
+        wd = torch.full((N, K), float("nan"), dtype=torch.float32, device="cuda")
+        lean.lean_dequant(fmt, Wd, wd, N, K)
+        torch.cuda.synchronize()
+        got = wd.cpu().numpy()
+        ref = oracle.dequant(fmt, W, N, K).astype(np.float32)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), (fmt, N, K)
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+def test_one_hot_bit_exact(lean, fmt):
+    """x = e_k: y[n] must equal w[n,k] exactly (one nonzero product)."""
+    be = syn.BLOCK_ELEMS[fmt]
+    N, K = 37, 5 * be
+    W, _ = syn.make_problem(fmt, N, K, 1, seed=(21, fmt))
+    ks = sorted(set([0, 1, 15, 16, 17, 31, be - 1, be, K // 2, K - 2, K - 1]))
+    x = np.zeros((len(ks), K), np.float32)
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+    w = oracle.dequant(fmt, W, N, K)
+    for M in (1, len(ks)):
+        y = run_gpu(fmt, W, x[:M], N, K)
+        assert np.array_equal(y, w[:, ks[:M]].T), (fmt, M)
+
+
+# ---- random problems: tolerance -------------------------------------------------
+
+SHAPES = [(1, 1, 1), (32, 1, 1), (33, 2, 1), (100, 9, 1), (960, 30, 1), (65, 43, 1),
+          (130, 7, 2), (50, 9, 3), (77, 12, 4), (64, 10, 7), (96, 17, 16), (40, 6, 17)]
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+@pytest.mark.parametrize("N,nblk,M", SHAPES)
+def test_parity_random(lean, fmt, N, nblk, M):
+    be = syn.BLOCK_ELEMS[fmt]
+    if fmt == syn.Q6_K:
+        nblk = max(1, nblk // 4)
+    K = nblk * be
+    W, x = syn.make_problem(fmt, N, K, M, seed=(22, fmt, N, K, M))
+    y = run_gpu(fmt, W, x, N, K)
+    y_ref, bound = oracle.qmatmul(fmt, W, x, N, K, threads=4)
+    check_close(y, y_ref, bound, "%s N=%d K=%d M=%d" % (syn.FORMAT_NAMES[fmt], N, K, M))
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+def test_deterministic_and_canary(lean, fmt):
+    """Same inputs -> same bits; nothing written outside y."""
+    torch = torch_cuda()
+    be = syn.BLOCK_ELEMS[fmt]
+    N, K, M = 70, 8 * be, 3
+    W, x = syn.make_problem(fmt, N, K, M, seed=(23, fmt))
+    Wd = lean.upload_packed(fmt, W, N, K)
+    xd = torch.from_numpy(x).cuda()
+    buf = torch.full((M * N + 64,), float("nan"), dtype=torch.float32, device="cuda")
+    lean.lean_qmatmul(fmt, Wd, xd, buf, N, K, M)
+    a = buf.clone()
+    lean.lean_qmatmul(fmt, Wd, xd, buf, N, K, M)
+    torch.cuda.synchronize()
+    assert torch.equal(a[:M * N].view(torch.int32), buf[:M * N].view(torch.int32))
+    assert torch.isnan(buf[M * N:]).all()
+    assert not torch.isnan(buf[:M * N]).any()
+
+
+# ---- argument errors are returned before any launch ----------------------------
+
+def test_argument_errors(lean):
+    torch = torch_cuda()
+    N, K = 32, 64
+    W, x = syn.make_problem(syn.Q4_0, N, K, 1, seed=(24,))
+    Wd = lean.upload_packed(syn.Q4_0, W, N, K)
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    f = lean._lib.lean_qmatmul
+    assert f(7, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, st) == lean.LEAN_ERR_FORMAT
+    assert f(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, 48, 1, st) == lean.LEAN_ERR_SHAPE
+    assert f(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), 0, K, 1, st) == lean.LEAN_ERR_SHAPE
+    assert f(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 0, st) == lean.LEAN_ERR_SHAPE
+    assert f(0, None, xd.data_ptr(), yd.data_ptr(), N, K, 1, st) == lean.LEAN_ERR_NULL
+    assert f(0, Wd.data_ptr(), xd.data_ptr() + 4, yd.data_ptr(), N, K, 1, st) == lean.LEAN_ERR_ALIGN
+    assert f(0, Wd.data_ptr() + 8, xd.data_ptr(), yd.data_ptr(), N, K, 1, st) == lean.LEAN_ERR_ALIGN
+    # a good call still works afterwards
+    assert f(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, st) == lean.LEAN_OK
+    torch.cuda.synchronize()
+
+
+def test_streams_and_graph_capture(lean):
+    """Calls run on the given stream and can be captured into a CUDA graph."""
+    torch = torch_cuda()
+    fmt, N, K = syn.Q4_0, 256, 512
+    W, x = syn.make_problem(fmt, N, K, 1, seed=(25,))
+    Wd = lean.upload_packed(fmt, W, N, K)
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.zeros((1, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        lean.lean_qmatmul(fmt, Wd, xd, yd, N, K, 1, s)  # warm-up outside capture
+        s.synchronize()
+        yd.zero_()
+        with torch.cuda.graph(g, stream=s):
+            lean.lean_qmatmul(fmt, Wd, xd, yd, N, K, 1, s)
+    g.replay()
+    torch.cuda.synchronize()
+    y_ref, bound = oracle.qmatmul(fmt, W, x, N, K)
+    check_close(yd.cpu().numpy().astype(np.float64), y_ref, bound, "graph replay")
