@@ -1,0 +1,476 @@
+"""Benchmark of the block-quantized weight x activation product on GB300.
+
+Default workload: one decode step of SmolLM2-360M's Q4_0 linears (32 layers x
+q/k/v/o/gate/up/down, M=1, a fresh seeded x per linear), i.e. 224 GEMVs and
+179.1 MB of algorithmic traffic per step.  A step runs every linear once from
+weights already resident in HBM; steps alternate between weight copies whose
+total exceeds twice the L2, so every step streams its weights from HBM.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the host cores instead.  `--sweep` also prints one line per workload for
+the other shapes (to stderr), which the default run does not.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from block_quantized_weight_dot_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = ("Q4_0 GEMV achieved HBM GB/s (% of GB300 peak) and decode-step linears/s, M=1")
+HBM_FALLBACK_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- helpers ---
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantized_weight_dot_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag):
+    """dram read+write bytes per launch recorded by an ncu capture under
+    profiles/, or None when absent or taken on different kernel sources."""
+    prof = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(prof):
+        return None
+    want = kernel_source_hash()
+    for f in sorted(os.listdir(prof)):
+        if not f.endswith((".md", ".txt")):
+            continue
+        text = open(os.path.join(prof, f)).read()
+        m = re.search(r"traffic_bytes_per_launch\[%s\]:\s*([0-9.eE+]+)\s+source_hash:\s*(\w+)"
+                      % re.escape(kernel_tag), text)
+        if m and m.group(2) == want:
+            return float(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 100 ms in the background."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        sel = [r for (t, r) in self.rows if t0 - 0.15 <= t <= t1 + 0.15]
+        note = "in timed region"
+        if not sel and self.rows:
+            # region shorter than the sampling period: nearest samples
+            sel = [r for (t, r) in sorted(self.rows, key=lambda tr: abs(tr[0] - (t0 + t1) / 2))[:3]]
+            note = "nearest samples (timed region shorter than the 100 ms sampling period)"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+        sm = [float(r[2]) for r in sel if len(r) > 9 and r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in sel if len(r) > 9 and r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sel if len(r) > 9 for i in range(4)
+                          if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(sel), "note": note}
+
+
+# -------------------------------------------------------------- workloads ---
+
+def workload_by_name(name):
+    table = {
+        "decode_stack": syn.smollm2_360m_decode_stack,
+        "gemv_960": syn.q4_0_gemv_960,
+        "tinyllama_q8_0": lambda: syn.tinyllama_gemv(syn.Q8_0),
+        "tinyllama_i8_b64": lambda: syn.tinyllama_gemv(syn.I8_B64),
+        "lm_head_q6_k": syn.qwen25_3b_lm_head,
+    }
+    for M in syn.QWEN25_3B_FFN_BATCHES:
+        table["qwen_ffn_M%d" % M] = (lambda M=M: syn.qwen25_3b_ffn(M))
+    return table[name]()
+
+
+class DeviceWorkload:
+    """Packed weights (several copies, > 2x L2 in total), x and y resident in HBM."""
+
+    def __init__(self, wl, device, l2_bytes, copies=None):
+        import torch
+        from block_quantized_weight_dot_gb300 import lean
+        self.wl, self.lean, self.torch = wl, lean, torch
+        self.lins = list(wl.linears)
+        packed, xs = [], []
+        for lin in self.lins:
+            W, x = lin.make()
+            packed.append(lean.lean_pack(lin.fmt, W, lin.N, lin.K))
+            xs.append(x)
+        self.canon_x = xs
+        per_copy = sum(p.size for p in packed)
+        self.copies = copies or max(2, int(np.ceil(2.2 * l2_bytes / per_copy)))
+        self.W = [[torch.from_numpy(p).to(device) for p in packed] for _ in range(self.copies)]
+        # one contiguous x buffer and one y buffer (host mirrors for e2e)
+        self.x_off, self.y_off = [], []
+        xo = yo = 0
+        for lin in self.lins:
+            self.x_off.append(xo)
+            self.y_off.append(yo)
+            xo += lin.M * lin.K + (-lin.M * lin.K) % 4   # keep every x 16-byte aligned
+            yo += lin.M * lin.N + (-lin.M * lin.N) % 4
+        x_host = np.zeros(xo, np.float32)
+        for lin, off, x in zip(self.lins, self.x_off, xs):
+            x_host[off:off + lin.M * lin.K] = x.reshape(-1)
+        self.x_host = torch.from_numpy(x_host).pin_memory()
+        self.y_host = torch.empty(yo, dtype=torch.float32).pin_memory()
+        self.x = self.x_host.to(device)
+        self.y = torch.empty(yo, dtype=torch.float32, device=device)
+        self.launches_per_step = None
+        self.flags = lean.LEAN_FLAG_EARLY_WEIGHTS
+
+    def run_step(self, copy, stream):
+        lean = self.lean
+        n = 0
+        for i, lin in enumerate(self.lins):
+            x = self.x.data_ptr() + 4 * self.x_off[i]
+            y = self.y.data_ptr() + 4 * self.y_off[i]
+            lean.lean_qmatmul_ex(lin.fmt, self.W[copy][i], x, y, lin.N, lin.K, lin.M,
+                                 self.flags, stream)
+            n += (lin.M + 15) // 16
+        self.launches_per_step = n
+
+    def capture(self, stream):
+        torch = self.torch
+        graphs = []
+        for c in range(self.copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    self.run_step(c, stream)
+            graphs.append(g)
+        return graphs
+
+
+# ----------------------------------------------------------------- GPU arm ---
+
+def time_gpu(args, wl):
+    import torch
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    dw = DeviceWorkload(wl, device, l2)
+    stream = torch.cuda.Stream(device)
+    # warm the library (plans, attributes) outside capture
+    with torch.cuda.stream(stream):
+        dw.run_step(0, stream)
+    stream.synchronize()
+    graphs = dw.capture(stream)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    # correctness spot check of the first linear against the oracle (rank 0)
+    spot = None
+    if rank == 0:
+        import oracle
+        lin = dw.lins[0]
+        graphs[0].replay()
+        torch.cuda.synchronize()
+        W, x = lin.make()
+        y_ref, bound = oracle.qmatmul(lin.fmt, W, x, lin.N, lin.K)
+        y = dw.y[dw.y_off[0]:dw.y_off[0] + lin.M * lin.N].cpu().numpy().reshape(lin.M, lin.N)
+        spot = bool(np.all(np.abs(y - y_ref) <= 1e-4 * bound + 1e-6))
+
+    for s in range(args.warmup):
+        graphs[s % dw.copies].replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for s in range(args.steps):
+            graphs[s % dw.copies].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+
+    # end to end: pinned host x -> device, the step, y -> pinned host, every step
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for s in range(2):
+            dw.x.copy_(dw.x_host, non_blocking=True)
+            graphs[s % dw.copies].replay()
+            dw.y_host.copy_(dw.y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for s in range(e_steps):
+            dw.x.copy_(dw.x_host, non_blocking=True)
+            graphs[s % dw.copies].replay()
+            dw.y_host.copy_(dw.y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+        dist.destroy_process_group()
+    return {"ms": ms, "e2e_ms": e2e_ms, "clocks": clocks, "launches": dw.launches_per_step,
+            "copies": dw.copies, "spot_ok": spot, "h2d": dw.x_host.numel() * 4,
+            "d2h": dw.y_host.numel() * 4, "l2": l2}
+
+
+# ----------------------------------------------------------------- CPU arm ---
+
+def oracle_inputs(wl):
+    return [(lin, lin.make()) for lin in wl.linears]
+
+
+def time_oracle(inputs, n_per_step, budget_s, start=0):
+    """The oracle as it stands, all host cores, on a bounded sample of the step:
+    whole linears in workload order (from `start`, wrapping) until the time
+    budget is spent (at least one)."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    done_bytes, elapsed, n_lin = 0, 0.0, 0
+    i = start
+    while n_lin == 0 or elapsed < budget_s:
+        lin, (W, x) = inputs[i % len(inputs)]
+        t = time.perf_counter()
+        oracle.qmatmul(lin.fmt, W, x, lin.N, lin.K, threads=cores)
+        elapsed += time.perf_counter() - t
+        done_bytes += lin.algorithmic_bytes
+        n_lin += 1
+        i += 1
+    return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d of the workload's linears (%d per step), fp64 scalar C, %d threads, %.2f s"
+                      % (n_lin, n_per_step, cores, elapsed),
+            "seconds": elapsed, "linears": n_lin, "next": i}
+
+
+# -------------------------------------------------------------------- main ---
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="lean", choices=["lean", "reference"])
+    ap.add_argument("--workload", default="decode_stack")
+    ap.add_argument("--sweep", action="store_true", help="also time every workload (stderr)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    wl = workload_by_name(args.workload)
+    peak, peak_kind = measured_peaks()
+    alg_bytes = wl.algorithmic_bytes
+    n_lin = len(wl.linears)
+    config = {"workload": wl.name, "linears_per_step": n_lin, "M": wl.linears[0].M,
+              "algorithmic_bytes_per_step": alg_bytes, "weight_bytes_per_step": wl.weight_bytes,
+              "inputs": "seeded synthetic, resident in HBM", "n_gpus": args.gpus}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        t0 = time.time()
+        inputs = oracle_inputs(wl)
+        per, nxt = [], 0
+        for s in range(args.warmup + args.steps):
+            r = time_oracle(inputs, n_lin, args.cpu_budget / max(1, args.steps), nxt)
+            nxt = r["next"]
+            if s >= args.warmup:
+                per.append(r)
+        gbs = float(np.mean([r["value"] for r in per]))
+        ms_step = alg_bytes / (gbs * 1e9) * 1e3
+        line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config,
+                "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": per[0]["cores"],
+                                 "kind": "oracle", "sample": per[0]["sample"] + " per step"},
+                "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "wall_s": time.time() - t0}
+        print(json.dumps(line), flush=True)
+        return
+
+    r = time_gpu(args, wl)
+    if rank != 0:
+        return
+    s_step = r["ms"] * 1e-3
+    gbs = alg_bytes / s_step / 1e9 * ws
+    linears_per_s = n_lin / s_step * ws
+    per_launch_bytes = alg_bytes / r["launches"]
+    per_launch_s = s_step / r["launches"]
+    achieved = per_launch_bytes / per_launch_s / 1e9
+    tag = "qmm_simt_q4_0_m1:" + wl.name
+    traffic = profiled_traffic(tag)
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        cpu = time_oracle(oracle_inputs(wl), n_lin, args.cpu_budget)
+        for k in ("seconds", "linears", "next"):
+            cpu.pop(k, None)
+    config.update({"l2_defeat": "weights rotate over %d copies (%.0f MB > 2x L2 of %.0f MB)"
+                   % (r["copies"], r["copies"] * wl.weight_bytes / 1e6, r["l2"] / 1e6),
+                   "graph": "one CUDA graph per weight copy; a step = one graph replay",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"})
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "config": config,
+        "linears_per_s": linears_per_s,
+        "frac_of_hbm_peak": gbs / ws / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "qmm_simt_kernel<Q4_0,1>", "launches_per_step": r["launches"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": alg_bytes / (r["e2e_ms"] * 1e-3) / 1e9 * ws, "unit": "GB/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "ms_per_step": r["e2e_ms"]},
+        "gpu_launches": r["launches"] * args.steps,
+        "clocks": r["clocks"],
+        "spot_check_vs_oracle": r["spot_ok"],
+    }
+    print(json.dumps(line), flush=True)
+
+    if args.sweep:
+        sweep(args)
+
+
+def sweep(args):
+    """Per-linear timings: one CUDA graph holding one call per weight copy,
+    the copies together larger than 2.2x L2, so every call streams from HBM."""
+    import torch
+    peak, _ = measured_peaks()
+    names = ["gemv_960", "tinyllama_q8_0", "tinyllama_i8_b64", "lm_head_q6_k"] + \
+            ["qwen_ffn_M%d" % M for M in syn.QWEN25_3B_FFN_BATCHES]
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    stream = torch.cuda.Stream()
+    for name in names:
+        wl = workload_by_name(name)
+        for lin in wl.linears:
+            one = syn.Workload(lin.name, (lin,))
+            dw = DeviceWorkload(one, torch.device("cuda"), l2)
+            with torch.cuda.stream(stream):
+                dw.run_step(0, stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    for c in range(dw.copies):
+                        dw.run_step(c, stream)
+            for i in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = 20
+            ev0.record(stream)
+            with torch.cuda.stream(stream):
+                for i in range(n):
+                    g.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            t = ev0.elapsed_time(ev1) / n / dw.copies * 1e-3
+            gbs = lin.algorithmic_bytes / t / 1e9
+            print(json.dumps({"sweep": name, "linear": lin.name, "fmt": syn.FORMAT_NAMES[lin.fmt],
+                              "N": lin.N, "K": lin.K, "M": lin.M, "us": round(t * 1e6, 3),
+                              "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "TFLOP/s": round(lin.flops / t / 1e12, 3),
+                              "launches": dw.launches_per_step, "copies": dw.copies}),
+                  file=sys.stderr, flush=True)
+            del dw, g
+            torch.cuda.empty_cache()
+
+
+if __name__ == "__main__":
+    main()

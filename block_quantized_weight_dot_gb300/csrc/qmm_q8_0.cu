@@ -3,6 +3,6 @@
 
 namespace lean {
 template lean_status qmm_fmt<Q8_0>(const Geom &, const uint8_t *, const float *, float *, int64_t,
-                                 cudaStream_t);
+                                 unsigned, cudaStream_t);
 template lean_status dequant_fmt<Q8_0>(const Geom &, const uint8_t *, float *, cudaStream_t);
 }  // namespace lean

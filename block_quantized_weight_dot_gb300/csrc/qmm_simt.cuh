@@ -209,7 +209,7 @@ __device__ __forceinline__ void compute_step(const StepFrag<FMT> &f, const float
 // A CTA owns rg row groups; each row group gets wpr warps that split the
 // CTA's steps.  Dynamic shared memory: MT * xs_stride floats of x, then
 // warps * MT * 32 floats of partial sums.
-template <int FMT, int MT>
+template <int FMT, int MT, bool DB>
 __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
     constexpr int SE = StepTraits<FMT>::ELEMS;
     constexpr int V = StepTraits<FMT>::VECS;
@@ -232,8 +232,16 @@ __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
     const int64_t qrow = g * a.qvec * kRowsPerGroup + lane;
     const int64_t srow = g * a.svec * kRowsPerGroup + lane;
 
+    // Programmatic dependent launch: let the next kernel on the stream start
+    // its own weight loads now; weights are never written by these kernels.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     StepFrag<FMT> fa, fb;
     if (w0 < w1) load_step<FMT>(fa, a, qrow, srow, w0);
+
+    // x may be produced by the preceding kernel: wait for it to complete
+    // (a no-op when the launch has no programmatic dependency).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // stage x[m][c0*SE .. min(c1*SE, K)) into shared memory
     float *xs = smem;
@@ -251,12 +259,20 @@ __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) tot[m] = 0.f;
 
-    for (int st = w0; st < w1; st += 2) {
-        if (st + 1 < w1) load_step<FMT>(fb, a, qrow, srow, st + 1);
-        compute_step<FMT, MT>(fa, xs + (st - c0) * SE, a.xs_stride, a.qvec - st * V, tot);
-        if (st + 2 < w1) load_step<FMT>(fa, a, qrow, srow, st + 2);
-        if (st + 1 < w1)
-            compute_step<FMT, MT>(fb, xs + (st + 1 - c0) * SE, a.xs_stride, a.qvec - (st + 1) * V, tot);
+    if (DB) {  // prefetch the next step while computing this one
+        for (int st = w0; st < w1; st += 2) {
+            if (st + 1 < w1) load_step<FMT>(fb, a, qrow, srow, st + 1);
+            compute_step<FMT, MT>(fa, xs + (st - c0) * SE, a.xs_stride, a.qvec - st * V, tot);
+            if (st + 2 < w1) load_step<FMT>(fa, a, qrow, srow, st + 2);
+            if (st + 1 < w1)
+                compute_step<FMT, MT>(fb, xs + (st + 1 - c0) * SE, a.xs_stride,
+                                      a.qvec - (st + 1) * V, tot);
+        }
+    } else {
+        for (int st = w0; st < w1; ++st) {
+            if (st > w0) load_step<FMT>(fa, a, qrow, srow, st);
+            compute_step<FMT, MT>(fa, xs + (st - c0) * SE, a.xs_stride, a.qvec - st * V, tot);
+        }
     }
 
     // reduce over the wpr warps of each row group: red[warp][m][lane]

@@ -37,7 +37,7 @@ template <int FMT> constexpr int step_elems() { return StepTraits<FMT>::ELEMS; }
 template <int FMT> constexpr int step_vecs() { return StepTraits<FMT>::VECS; }
 
 struct Plan {
-    int cl, rg, wpr, mt;
+    int cl, rg, wpr, mt, per_warp;
     int64_t ctas;
     size_t smem;
     int xs_stride;
@@ -71,6 +71,7 @@ bool plan_simt(const Geom &g, int mt, Plan *p) {
     p->rg = rg;
     p->wpr = wpr;
     p->mt = mt;
+    p->per_warp = per_warp;
     p->ctas = (g.groups + rg - 1) / rg * cl;
     p->smem = smem;
     p->xs_stride = xs_stride;
@@ -79,7 +80,7 @@ bool plan_simt(const Geom &g, int mt, Plan *p) {
 
 template <int FMT, int MT>
 lean_status launch_simt(const Geom &g, const uint8_t *W, const float *x, float *y, int M,
-                        cudaStream_t stream) {
+                        unsigned flags, cudaStream_t stream) {
     Plan p;
     if (!plan_simt<FMT>(g, MT, &p)) return LEAN_ERR_SHAPE;
     SimtArgs a;
@@ -98,7 +99,9 @@ lean_status launch_simt(const Geom &g, const uint8_t *W, const float *x, float *
     a.rg = p.rg;
     a.wpr = p.wpr;
     a.xs_stride = p.xs_stride;
-    auto kern = qmm_simt_kernel<FMT, MT>;
+    // double-buffer the steps only when a warp has several and registers allow
+    auto kern = (p.per_warp >= 2 && MT <= 2) ? qmm_simt_kernel<FMT, MT, true>
+                                              : qmm_simt_kernel<FMT, MT, false>;
     if (p.smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
             cudaSuccess)
@@ -110,33 +113,40 @@ lean_status launch_simt(const Geom &g, const uint8_t *W, const float *x, float *
     cfg.blockDim = dim3((unsigned)(32 * p.rg * p.wpr), 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    int na = 0;
     if (p.cl > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = p.cl;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = p.cl;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    if (flags & LEAN_FLAG_EARLY_WEIGHTS) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return LEAN_ERR_CUDA;
     return LEAN_OK;
 }
 
 template <int FMT>
 lean_status qmm_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
-                    cudaStream_t stream) {
+                    unsigned flags, cudaStream_t stream) {
     // M rows of x in tiles of at most 16; each tile re-streams the weights.
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int mt = (int)std::min<int64_t>(16, M - m0);
         const float *xt = x + m0 * g.K;
         float *yt = y + m0 * g.N;
         lean_status s;
-        if (mt == 1) s = launch_simt<FMT, 1>(g, W, xt, yt, mt, stream);
-        else if (mt == 2) s = launch_simt<FMT, 2>(g, W, xt, yt, mt, stream);
-        else if (mt <= 4) s = launch_simt<FMT, 4>(g, W, xt, yt, mt, stream);
-        else if (mt <= 8) s = launch_simt<FMT, 8>(g, W, xt, yt, mt, stream);
-        else s = launch_simt<FMT, 16>(g, W, xt, yt, mt, stream);
+        if (mt == 1) s = launch_simt<FMT, 1>(g, W, xt, yt, mt, flags, stream);
+        else if (mt == 2) s = launch_simt<FMT, 2>(g, W, xt, yt, mt, flags, stream);
+        else if (mt <= 4) s = launch_simt<FMT, 4>(g, W, xt, yt, mt, flags, stream);
+        else if (mt <= 8) s = launch_simt<FMT, 8>(g, W, xt, yt, mt, flags, stream);
+        else s = launch_simt<FMT, 16>(g, W, xt, yt, mt, flags, stream);
         if (s != LEAN_OK) return s;
     }
     return LEAN_OK;

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "liblean_qmatmul.so")
 
 LEAN_Q4_0, LEAN_Q8_0, LEAN_I8_B64, LEAN_Q6_K = 0, 1, 2, 3
 LEAN_OK, LEAN_ERR_FORMAT, LEAN_ERR_SHAPE, LEAN_ERR_NULL, LEAN_ERR_ALIGN, LEAN_ERR_CUDA = range(6)
+LEAN_FLAG_EARLY_WEIGHTS = 1
 
 # every symbol the header declares, with (restype, argtypes)
 _i64, _int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
@@ -30,6 +31,7 @@ SIGNATURES = {
     "lean_unpack_canonical": (_int, [_int, _vp, _vp, _i64, _i64]),
     "lean_dequant": (_int, [_int, _vp, _vp, _i64, _i64, _vp]),
     "lean_qmatmul": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "lean_qmatmul_ex": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp]),
     "lean_status_str": (ctypes.c_char_p, [_int]),
 }
 
@@ -144,6 +146,13 @@ def lean_qmatmul(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,
     """y[M][N] = x[M][K] . W[N][K]^T on the device, asynchronously on `stream`."""
     _check("lean_qmatmul", _lib.lean_qmatmul(fmt, _addr(W_packed_dev), _addr(x_dev),
                                              _addr(y_dev), N, K, M, _stream(stream)))
+
+
+def lean_qmatmul_ex(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,
+                    flags: int = 0, stream=None) -> None:
+    """lean_qmatmul with launch flags (LEAN_FLAG_EARLY_WEIGHTS)."""
+    _check("lean_qmatmul_ex", _lib.lean_qmatmul_ex(fmt, _addr(W_packed_dev), _addr(x_dev),
+                                                   _addr(y_dev), N, K, M, flags, _stream(stream)))
 
 
 # ---- torch conveniences (device memory via PyTorch; compute via the library) ----

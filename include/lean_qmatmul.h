@@ -128,6 +128,25 @@ lean_status lean_dequant(int fmt, const void *W_packed_dev, float *w_dev,
 lean_status lean_qmatmul(int fmt, const void *W_packed_dev, const float *x_dev,
                          float *y_dev, int64_t N, int64_t K, int64_t M, void *stream);
 
+/* Flags for lean_qmatmul_ex. */
+enum {
+    /* Programmatic dependent launch: the kernel may be scheduled, and may start
+     * streaming W, before the preceding kernel on `stream` has finished; it
+     * reads x and writes y only after that kernel has completed and its writes
+     * are visible.  Consecutive products on one stream then overlap their
+     * weight streaming with each other's tails, which is what a decode step
+     * of many small GEMVs needs.  Set it only when the preceding kernel on the
+     * stream does not write W (weights uploaded by cudaMemcpy, or resident
+     * model weights, are fine). */
+    LEAN_FLAG_EARLY_WEIGHTS = 1u
+};
+
+/* lean_qmatmul with launch flags (LEAN_FLAG_*; unknown bits are rejected
+ * with LEAN_ERR_FORMAT).  flags = 0 is exactly lean_qmatmul. */
+lean_status lean_qmatmul_ex(int fmt, const void *W_packed_dev, const float *x_dev,
+                            float *y_dev, int64_t N, int64_t K, int64_t M,
+                            unsigned flags, void *stream);
+
 /* Static description of a status code. */
 const char *lean_status_str(int status);
 

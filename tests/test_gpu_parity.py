@@ -138,3 +138,68 @@ def test_streams_and_graph_capture(lean):
     torch.cuda.synchronize()
     y_ref, bound = oracle.qmatmul(fmt, W, x, N, K)
     check_close(yd.cpu().numpy().astype(np.float64), y_ref, bound, "graph replay")
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_early_weights_chain_orders_x(lean, M):
+    """A chain y_{i+1} = W_i y_i with programmatic dependent launch: each
+    product must read its x only after the previous one wrote it.  The chain is
+    run with and without the flag (and inside a CUDA graph); results must match
+    bit for bit, and the buffers start as NaN so a premature read shows."""
+    torch = torch_cuda()
+    fmt, N = syn.Q4_0, 960
+    steps = 24
+    Ws = []
+    for i in range(steps):
+        W, _ = syn.make_problem(fmt, N, N, 1, seed=(26, i))
+        Ws.append(lean.upload_packed(fmt, W, N, N))
+    _, x0 = syn.make_problem(fmt, N, N, M, seed=(27,))
+    x0d = torch.from_numpy(x0 / np.float32(30.0)).cuda()
+
+    def chain(flags, stream):
+        bufs = [torch.full((M, N), float("nan"), device="cuda") for _ in range(steps)]
+        torch.cuda.synchronize()
+        cur = x0d
+        for i in range(steps):
+            lean.lean_qmatmul_ex(fmt, Ws[i], cur, bufs[i], N, N, M, flags, stream)
+            cur = bufs[i]
+        return bufs
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ref = chain(0, s)
+        pdl = chain(lean.LEAN_FLAG_EARLY_WEIGHTS, s)
+    s.synchronize()
+    for a, b in zip(ref, pdl):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.isfinite(ref[-1]).all()
+    # the same chain captured into a graph
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        bufs = [torch.full((M, N), float("nan"), device="cuda") for _ in range(steps)]
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            cur = x0d
+            for i in range(steps):
+                lean.lean_qmatmul_ex(fmt, Ws[i], cur, bufs[i], N, N, M,
+                                     lean.LEAN_FLAG_EARLY_WEIGHTS, s)
+                cur = bufs[i]
+    for _ in range(3):
+        for b in bufs:
+            b.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(ref, bufs):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_flags_rejected(lean):
+    torch = torch_cuda()
+    N, K = 32, 64
+    W, x = syn.make_problem(syn.Q4_0, N, K, 1, seed=(28,))
+    Wd = lean.upload_packed(syn.Q4_0, W, N, K)
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty((1, N), device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, 2,
+                                     st) == lean.LEAN_ERR_FORMAT
