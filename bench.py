@@ -186,16 +186,39 @@ class DeviceWorkload:
         self.y = torch.empty(yo, dtype=torch.float32, device=device)
         self.launches_per_step = None
         self.flags = lean.LEAN_FLAG_EARLY_WEIGHTS
+        # one workspace, zeroed once: consecutive calls on the stream share it
+        fmt0 = self.lins[0].fmt
+        self.batch = None
+        if (len(self.lins) > 1 and len(self.lins) <= lean.LEAN_MAX_BATCH
+                and all(l.M == 1 and l.fmt == fmt0 for l in self.lins)):
+            self.batch = []
+            for c in range(self.copies):
+                items = [(self.W[c][i], self.x.data_ptr() + 4 * self.x_off[i],
+                          self.y.data_ptr() + 4 * self.y_off[i], l.N, l.K)
+                         for i, l in enumerate(self.lins)]
+                self.batch.append(lean.make_problems(items))
+            self.ws_bytes = lean.lean_batch_workspace_bytes(fmt0, self.batch[0])
+        else:
+            self.ws_bytes = max(lean.lean_qmatmul_workspace_bytes(l.fmt, l.N, l.K, l.M)
+                                for l in self.lins)
+        self.ws = torch.zeros(max(256, self.ws_bytes), dtype=torch.uint8, device=device)
 
     def run_step(self, copy, stream):
+        """One pass over every linear: a single batched launch when all linears
+        are M = 1 products of one format, otherwise one call per linear."""
         lean = self.lean
+        if self.batch is not None:
+            lean.lean_qmatmul_batch(self.lins[0].fmt, self.batch[copy], self.flags, self.ws,
+                                    self.ws_bytes, stream)
+            self.launches_per_step = 1
+            return
         n = 0
         for i, lin in enumerate(self.lins):
             x = self.x.data_ptr() + 4 * self.x_off[i]
             y = self.y.data_ptr() + 4 * self.y_off[i]
-            lean.lean_qmatmul_ex(lin.fmt, self.W[copy][i], x, y, lin.N, lin.K, lin.M,
-                                 self.flags, stream)
-            n += (lin.M + 15) // 16
+            lean.lean_qmatmul_ws(lin.fmt, self.W[copy][i], x, y, lin.N, lin.K, lin.M,
+                                 self.flags, self.ws, self.ws_bytes, stream)
+            n += 1 if lin.M == 1 else (lin.M + 15) // 16
         self.launches_per_step = n
 
     def capture(self, stream):
@@ -299,7 +322,11 @@ def time_gpu(args, wl):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, e2e_ms = float(t[0]), float(t[1])
         dist.destroy_process_group()
+    kernel = ("qmm_stream_kernel<%s,%s> (TMA ring, %s)"
+              % (syn.FORMAT_NAMES[dw.lins[0].fmt], "batch" if dw.batch is not None else "1",
+                 "one launch per step" if dw.batch is not None else "one launch per linear"))
     return {"ms": ms, "e2e_ms": e2e_ms, "clocks": clocks, "launches": dw.launches_per_step,
+            "kernel": kernel,
             "copies": dw.copies, "spot_ok": spot, "h2d": dw.x_host.numel() * 4,
             "d2h": dw.y_host.numel() * 4, "l2": l2}
 
@@ -389,7 +416,7 @@ def main():
     per_launch_bytes = alg_bytes / r["launches"]
     per_launch_s = s_step / r["launches"]
     achieved = per_launch_bytes / per_launch_s / 1e9
-    tag = "qmm_simt_q4_0_m1:" + wl.name
+    tag = "qmm_stream:" + wl.name
     traffic = profiled_traffic(tag)
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
@@ -411,7 +438,7 @@ def main():
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "qmm_simt_kernel<Q4_0,1>", "launches_per_step": r["launches"]},
+                     "kernel": r["kernel"], "launches_per_step": r["launches"]},
         "cpu_baseline": cpu,
         "e2e": {"value": alg_bytes / (r["e2e_ms"] * 1e-3) / 1e9 * ws, "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],

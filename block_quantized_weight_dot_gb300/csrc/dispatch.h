@@ -1,0 +1,45 @@
+// dispatch.h -- what the C-ABI translation unit needs from the per-format
+// kernel translation units (qmm_<fmt>.cu): problem descriptors, the workspace
+// layout and the per-format entry templates.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lean_qmatmul.h"
+#include "layout.h"
+
+namespace lean {
+
+constexpr int kMaxBatch = LEAN_MAX_BATCH;  // problems per batched launch
+constexpr int kMaxStreamCtas = 256;        // CTAs of one streaming launch, at most
+
+struct HostProb {
+    const uint8_t *W;
+    const float *x;
+    float *y;
+    Geom g;
+};
+
+// Workspace of the balanced (stream-K) GEMV: per-CTA partial sums of row
+// groups split between CTAs, then one arrival counter per row group.
+struct WorkspaceLayout {
+    int64_t part_off, cnt_off, total;
+};
+inline WorkspaceLayout workspace_layout(int64_t groups) {
+    WorkspaceLayout w;
+    w.part_off = 0;
+    w.cnt_off = (int64_t)kMaxStreamCtas * 2 * 32 * 4;
+    w.total = (w.cnt_off + groups * 4 + 255) / 256 * 256;
+    return w;
+}
+
+template <int FMT>
+lean_status simt_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
+                     unsigned flags, cudaStream_t stream);
+template <int FMT>
+lean_status dequant_fmt(const Geom &g, const uint8_t *W, float *w, cudaStream_t stream);
+template <int FMT>
+lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
+                       unsigned *err, cudaStream_t stream);
+
+}  // namespace lean

@@ -1,0 +1,279 @@
+// launch.cuh -- launch planning for the product kernels.  Included by one
+// translation unit per weight format (qmm_<fmt>.cu), each of which
+// instantiates the entry templates declared in dispatch.h.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "../../include/lean_qmatmul.h"
+#include "dispatch.h"
+#include "layout.h"
+#include "qmm_simt.cuh"
+#include "qmm_stream.cuh"
+
+namespace lean {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxWarpsPerCta = 16;
+constexpr int kMaxCluster = 8;
+constexpr size_t kMaxSimtSmem = 200 * 1024;
+
+inline int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// Per-device SM count, read once.
+inline int sm_count() {
+    static std::atomic<int> cache[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0) return 148;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// Raise a kernel's dynamic shared memory limit once per device.
+template <typename Kern>
+inline bool ensure_smem(Kern kern, size_t bytes, std::atomic<uint64_t> &done) {
+    if (bytes <= 48 * 1024) return true;
+    const int dev = current_device();
+    if (dev < 0) return false;
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_relaxed) & bit) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+        return false;
+    done.fetch_or(bit, std::memory_order_relaxed);
+    return true;
+}
+
+inline void fill_launch(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int cluster,
+                        unsigned flags) {
+    int na = 0;
+    if (cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (flags & LEAN_FLAG_EARLY_WEIGHTS) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+}
+
+// ------------------------------------------------------------ CUDA-core path ---
+
+struct SimtPlan {
+    int cl, rg, wpr;
+    int64_t ctas;
+    size_t smem;
+    int xs_stride;
+};
+
+// Aim for about 16 resident warps per SM with every warp owning a run of
+// blocks; split K over the warps of a CTA first, then over a cluster when x
+// does not fit one CTA's shared memory or one CTA has too few warps.
+template <int FMT>
+bool plan_simt(const Geom &g, int mt, SimtPlan *p) {
+    constexpr int E = BlockTraits<FMT>::E;
+    const int64_t target = (int64_t)sm_count() * 16;
+    int64_t want = (target + g.groups - 1) / g.groups;  // warps per row group
+    want = std::max<int64_t>(1, std::min<int64_t>(want, g.blocks));
+    const int64_t per_warp = (g.blocks + want - 1) / want;  // blocks per warp
+    const int wtot = (int)((g.blocks + per_warp - 1) / per_warp);
+    int cl = std::min(kMaxCluster, (wtot + kMaxWarpsPerCta - 1) / kMaxWarpsPerCta);
+    auto slice_floats = [&](int c) { return (int)(((g.blocks + c - 1) / c) * E); };
+    while (cl < kMaxCluster && (size_t)mt * slice_floats(cl) * 4 > kMaxSimtSmem / 2) ++cl;
+    const int wpr = std::max(1, std::min(kMaxWarpsPerCta, (wtot + cl - 1) / cl));
+    int rg = 1;
+    while (rg * 2 * wpr <= 8 && rg * 2 <= g.groups) rg *= 2;
+    const int xs_stride = slice_floats(cl);
+    const size_t smem = (size_t)mt * xs_stride * 4 + (size_t)rg * wpr * mt * 32 * 4;
+    if (smem > kMaxSimtSmem) return false;
+    p->cl = cl;
+    p->rg = rg;
+    p->wpr = wpr;
+    p->ctas = (g.groups + rg - 1) / rg * cl;
+    p->smem = smem;
+    p->xs_stride = xs_stride;
+    return true;
+}
+
+inline SimtArgs simt_args(const Geom &g, const uint8_t *W, const float *x, float *y, int M) {
+    SimtArgs a = {};
+    a.W = W;
+    a.x = x;
+    a.y = y;
+    a.N = (int)g.N;
+    a.K = (int)g.K;
+    a.M = M;
+    a.groups = g.groups;
+    a.blocks = g.blocks;
+    a.steps = g.steps;
+    a.last_blocks = g.last_blocks;
+    a.step_vecs = g.step_vecs;
+    a.group_vecs = g.group_vecs;
+    a.mg = make_magic();
+    return a;
+}
+
+template <int FMT, int MT>
+lean_status launch_simt(const Geom &g, const uint8_t *W, const float *x, float *y, int M,
+                        unsigned flags, cudaStream_t stream) {
+    static std::atomic<uint64_t> smem_done{0};
+    SimtPlan p;
+    if (!plan_simt<FMT>(g, MT, &p)) return LEAN_ERR_SHAPE;
+    if (p.ctas > INT32_MAX) return LEAN_ERR_SHAPE;
+    SimtArgs a = simt_args(g, W, x, y, M);
+    a.cl = p.cl;
+    a.rg = p.rg;
+    a.wpr = p.wpr;
+    a.xs_stride = p.xs_stride;
+    auto kern = qmm_simt_kernel<FMT, MT>;
+    if (!ensure_smem(kern, p.smem, smem_done)) return LEAN_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.ctas, 1, 1);
+    cfg.blockDim = dim3((unsigned)(32 * p.rg * p.wpr), 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    fill_launch(cfg, attr, p.cl, flags);
+    return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
+}
+
+template <int FMT>
+lean_status simt_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
+                     unsigned flags, cudaStream_t stream) {
+    // M rows of x in tiles of at most 16; each tile re-streams the weights
+    for (int64_t m0 = 0; m0 < M; m0 += 16) {
+        const int mt = (int)std::min<int64_t>(16, M - m0);
+        const float *xt = x + m0 * g.K;
+        float *yt = y + m0 * g.N;
+        lean_status s;
+        if (mt <= 2) s = launch_simt<FMT, 2>(g, W, xt, yt, mt, flags, stream);
+        else if (mt <= 4) s = launch_simt<FMT, 4>(g, W, xt, yt, mt, flags, stream);
+        else if (mt <= 8) s = launch_simt<FMT, 8>(g, W, xt, yt, mt, flags, stream);
+        else s = launch_simt<FMT, 16>(g, W, xt, yt, mt, flags, stream);
+        if (s != LEAN_OK) return s;
+    }
+    return LEAN_OK;
+}
+
+template <int FMT>
+lean_status dequant_fmt(const Geom &g, const uint8_t *W, float *w, cudaStream_t stream) {
+    SimtArgs a = simt_args(g, W, nullptr, nullptr, 0);
+    const int64_t items = g.groups * g.blocks;  // one warp each
+    const int64_t blocks = (items + 7) / 8;
+    if (blocks > INT32_MAX) return LEAN_ERR_SHAPE;
+    dequant_kernel<FMT><<<(unsigned)blocks, 256, 0, stream>>>(a, w);
+    return cudaGetLastError() == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
+}
+
+// -------------------------------------------------------------- stream path ---
+
+// Steps and groups of a problem list; false when the list is too long.
+inline bool stream_totals(const HostProb *ph, int n, int64_t *steps, int64_t *groups) {
+    if (n < 1 || n > kMaxBatch) return false;
+    int64_t t = 0, gg = 0;
+    for (int i = 0; i < n; ++i) {
+        t += ph[i].g.groups * ph[i].g.steps;
+        gg += ph[i].g.groups;
+    }
+    *steps = t;
+    *groups = gg;
+    return true;
+}
+
+inline int64_t stream_workspace_bytes(const HostProb *ph, int n) {
+    int64_t steps, groups;
+    if (!stream_totals(ph, n, &steps, &groups)) return -1;
+    return workspace_layout(groups).total;
+}
+
+template <int FMT, int NP>
+lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
+                          unsigned *err, cudaStream_t stream) {
+    using C = StreamCfg<FMT>;
+    using L = StreamLayout<FMT>;
+    static std::atomic<uint64_t> smem_done{0};
+    StreamArgs<NP> a;
+    a.nprob = n;
+    int64_t steps = 0, groups = 0;
+    for (int i = 0; i < n; ++i) {
+        const Geom &g = ph[i].g;
+        StreamProb &p = a.p[i];
+        p.W = ph[i].W;
+        p.x = ph[i].x;
+        p.y = ph[i].y;
+        p.N = (int)g.N;
+        p.K = (int)g.K;
+        p.steps = g.steps;
+        p.last_blocks = g.last_blocks;
+        p.group_vecs = g.group_vecs;
+        p.groups = g.groups;
+        p.step0 = steps;
+        p.group0 = groups;
+        steps += g.groups * g.steps;
+        groups += g.groups;
+    }
+    a.total_steps = steps;
+    a.total_groups = groups;
+    a.mg = make_magic();
+    a.err = err;
+    const int64_t sms = std::min<int64_t>(sm_count(), kMaxStreamCtas);
+    if (ws != nullptr) {
+        const WorkspaceLayout wl = workspace_layout(groups);
+        if (ws_bytes < wl.total) return LEAN_ERR_SHAPE;
+        a.balanced = 1;
+        a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(sms, (steps + C::KS - 1) / C::KS));
+        a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + wl.part_off);
+        a.cnt = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + wl.cnt_off);
+    } else {
+        a.balanced = 0;
+        a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(sms, groups));
+        a.part = nullptr;
+        a.cnt = nullptr;
+    }
+    auto kern = qmm_stream_kernel<FMT, NP>;
+    if (!ensure_smem(kern, L::SMEM, smem_done)) return LEAN_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.ctas, 1, 1);
+    cfg.blockDim = dim3(kStreamThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    fill_launch(cfg, attr, 1, flags);
+    return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
+}
+
+template <int FMT>
+lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
+                       unsigned *err, cudaStream_t stream) {
+    int64_t steps, groups;
+    if (!stream_totals(ph, n, &steps, &groups)) return LEAN_ERR_SHAPE;
+    if (n == 1) return launch_stream<FMT, 1>(ph, n, flags, ws, ws_bytes, err, stream);
+    return launch_stream<FMT, kMaxBatch>(ph, n, flags, ws, ws_bytes, err, stream);
+}
+
+}  // namespace lean
+
+// explicit instantiation of a format's entry templates (use inside namespace lean)
+#define LEAN_INSTANTIATE(FMT)                                                                  \
+    template lean_status simt_fmt<FMT>(const Geom &, const uint8_t *, const float *, float *,  \
+                                       int64_t, unsigned, cudaStream_t);                       \
+    template lean_status dequant_fmt<FMT>(const Geom &, const uint8_t *, float *, cudaStream_t); \
+    template lean_status stream_fmt<FMT>(const HostProb *, int, unsigned, void *, int64_t,     \
+                                         unsigned *, cudaStream_t);

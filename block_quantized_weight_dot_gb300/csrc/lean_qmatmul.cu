@@ -1,53 +1,142 @@
 // lean_qmatmul.cu -- C ABI entry points for the device calls: argument
-// checks and dispatch by format.  The kernels and their launch planning live
-// in one translation unit per format (qmm_<fmt>.cu).
+// checks and dispatch by format and M.  The kernels and their launch
+// planning live in one translation unit per format (qmm_<fmt>.cu).
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/lean_qmatmul.h"
+#include "dispatch.h"
 #include "layout.h"
-
-namespace lean {
-template <int FMT>
-lean_status qmm_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
-                    unsigned flags, cudaStream_t stream);
-template <int FMT>
-lean_status dequant_fmt(const Geom &g, const uint8_t *W, float *w, cudaStream_t stream);
-}  // namespace lean
 
 using namespace lean;
 
+// Device error word written by kernels whose bounded waits time out.
+__device__ unsigned lean_error_word;
+
 namespace {
+
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
-}  // namespace
 
-extern "C" {
+// Device address of the error word on the current device (looked up once).
+unsigned *error_word() {
+    static std::atomic<unsigned *> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    unsigned *p = cache[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, lean_error_word) != cudaSuccess) return nullptr;
+        p = static_cast<unsigned *>(a);
+        cache[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
 
-lean_status lean_qmatmul_ex(int fmt, const void *W_packed_dev, const float *x_dev, float *y_dev,
-                            int64_t N, int64_t K, int64_t M, unsigned flags, void *stream) {
-    if (block_elems(fmt) == 0) return LEAN_ERR_FORMAT;
-    Geom g;
-    if (M <= 0 || !make_geom(fmt, N, K, &g)) return LEAN_ERR_SHAPE;
-    if (M > ((int64_t)1 << 31) / std::max<int64_t>(K, N)) return LEAN_ERR_SHAPE;
-    if (!W_packed_dev || !x_dev || !y_dev) return LEAN_ERR_NULL;
-    if (!aligned(W_packed_dev, 16) || !aligned(x_dev, 16) || !aligned(y_dev, 4)) return LEAN_ERR_ALIGN;
-    if (flags & ~(unsigned)LEAN_FLAG_EARLY_WEIGHTS) return LEAN_ERR_FORMAT;
-    cudaGetLastError();  // start from a clean error state
-    const uint8_t *W = (const uint8_t *)W_packed_dev;
-    cudaStream_t s = (cudaStream_t)stream;
+template <int FMT>
+lean_status run_stream(const HostProb *ph, int n, unsigned flags, void *ws, int64_t wsb,
+                       cudaStream_t s) {
+    unsigned *err = error_word();
+    if (!err) return LEAN_ERR_CUDA;
+    return stream_fmt<FMT>(ph, n, flags, ws, wsb, err, s);
+}
+
+lean_status dispatch_stream(int fmt, const HostProb *ph, int n, unsigned flags, void *ws,
+                            int64_t wsb, cudaStream_t s) {
     switch (fmt) {
-    case LEAN_Q4_0: return qmm_fmt<Q4_0>(g, W, x_dev, y_dev, M, flags, s);
-    case LEAN_Q8_0: return qmm_fmt<Q8_0>(g, W, x_dev, y_dev, M, flags, s);
-    case LEAN_I8_B64: return qmm_fmt<I8_B64>(g, W, x_dev, y_dev, M, flags, s);
-    case LEAN_Q6_K: return qmm_fmt<Q6_K>(g, W, x_dev, y_dev, M, flags, s);
+    case LEAN_Q4_0: return run_stream<Q4_0>(ph, n, flags, ws, wsb, s);
+    case LEAN_Q8_0: return run_stream<Q8_0>(ph, n, flags, ws, wsb, s);
+    case LEAN_I8_B64: return run_stream<I8_B64>(ph, n, flags, ws, wsb, s);
+    case LEAN_Q6_K: return run_stream<Q6_K>(ph, n, flags, ws, wsb, s);
     }
     return LEAN_ERR_FORMAT;
 }
 
+lean_status check_product(int fmt, const void *W, const float *x, const float *y, int64_t N,
+                          int64_t K, int64_t M, unsigned flags, Geom *g) {
+    if (block_elems(fmt) == 0) return LEAN_ERR_FORMAT;
+    if (M <= 0 || !make_geom(fmt, N, K, g)) return LEAN_ERR_SHAPE;
+    if (M > ((int64_t)1 << 31) / std::max<int64_t>(K, N)) return LEAN_ERR_SHAPE;
+    if (!W || !x || !y) return LEAN_ERR_NULL;
+    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return LEAN_ERR_ALIGN;
+    if (flags & ~(unsigned)LEAN_FLAG_EARLY_WEIGHTS) return LEAN_ERR_FORMAT;
+    return LEAN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_dev, float *y_dev,
+                            int64_t N, int64_t K, int64_t M, unsigned flags, void *workspace,
+                            int64_t workspace_bytes, void *stream) {
+    Geom g;
+    lean_status st = check_product(fmt, W_packed_dev, x_dev, y_dev, N, K, M, flags, &g);
+    if (st != LEAN_OK) return st;
+    if (workspace && !aligned(workspace, 256)) return LEAN_ERR_ALIGN;
+    cudaGetLastError();  // start from a clean error state
+    const uint8_t *W = (const uint8_t *)W_packed_dev;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (M == 1) {
+        HostProb hp = {W, x_dev, y_dev, g};
+        return dispatch_stream(fmt, &hp, 1, flags, workspace, workspace_bytes, s);
+    }
+    switch (fmt) {
+    case LEAN_Q4_0: return simt_fmt<Q4_0>(g, W, x_dev, y_dev, M, flags, s);
+    case LEAN_Q8_0: return simt_fmt<Q8_0>(g, W, x_dev, y_dev, M, flags, s);
+    case LEAN_I8_B64: return simt_fmt<I8_B64>(g, W, x_dev, y_dev, M, flags, s);
+    case LEAN_Q6_K: return simt_fmt<Q6_K>(g, W, x_dev, y_dev, M, flags, s);
+    }
+    return LEAN_ERR_FORMAT;
+}
+
+lean_status lean_qmatmul_ex(int fmt, const void *W_packed_dev, const float *x_dev, float *y_dev,
+                            int64_t N, int64_t K, int64_t M, unsigned flags, void *stream) {
+    return lean_qmatmul_ws(fmt, W_packed_dev, x_dev, y_dev, N, K, M, flags, nullptr, 0, stream);
+}
+
 lean_status lean_qmatmul(int fmt, const void *W_packed_dev, const float *x_dev, float *y_dev,
                          int64_t N, int64_t K, int64_t M, void *stream) {
-    return lean_qmatmul_ex(fmt, W_packed_dev, x_dev, y_dev, N, K, M, 0u, stream);
+    return lean_qmatmul_ws(fmt, W_packed_dev, x_dev, y_dev, N, K, M, 0u, nullptr, 0, stream);
+}
+
+int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M) {
+    Geom g;
+    if (M <= 0 || !make_geom(fmt, N, K, &g)) return -1;
+    if (M > 1) return 0;
+    return workspace_layout(g.groups).total;
+}
+
+int64_t lean_batch_workspace_bytes(int fmt, int count, const lean_problem *problems) {
+    if (count < 1 || count > LEAN_MAX_BATCH || !problems) return -1;
+    int64_t groups = 0;
+    for (int i = 0; i < count; ++i) {
+        Geom g;
+        if (!make_geom(fmt, problems[i].N, problems[i].K, &g)) return -1;
+        groups += g.groups;
+    }
+    return workspace_layout(groups).total;
+}
+
+lean_status lean_qmatmul_batch(int fmt, int count, const lean_problem *problems, unsigned flags,
+                               void *workspace, int64_t workspace_bytes, void *stream) {
+    if (block_elems(fmt) == 0) return LEAN_ERR_FORMAT;
+    if (count < 1 || count > LEAN_MAX_BATCH) return LEAN_ERR_SHAPE;
+    if (!problems) return LEAN_ERR_NULL;
+    if (workspace && !aligned(workspace, 256)) return LEAN_ERR_ALIGN;
+    HostProb hp[LEAN_MAX_BATCH];
+    for (int i = 0; i < count; ++i) {
+        const lean_problem &p = problems[i];
+        lean_status st = check_product(fmt, p.W, p.x, p.y, p.N, p.K, 1, flags, &hp[i].g);
+        if (st != LEAN_OK) return st;
+        hp[i].W = (const uint8_t *)p.W;
+        hp[i].x = p.x;
+        hp[i].y = p.y;
+    }
+    cudaGetLastError();
+    return dispatch_stream(fmt, hp, count, flags, workspace, workspace_bytes,
+                           (cudaStream_t)stream);
 }
 
 lean_status lean_dequant(int fmt, const void *W_packed_dev, float *w_dev, int64_t N, int64_t K,
@@ -67,6 +156,18 @@ lean_status lean_dequant(int fmt, const void *W_packed_dev, float *w_dev, int64_
     case LEAN_Q6_K: return dequant_fmt<Q6_K>(g, W, w_dev, s);
     }
     return LEAN_ERR_FORMAT;
+}
+
+unsigned lean_device_error(int clear) {
+    unsigned v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return 0xFFFFFFFFu;
+    if (cudaMemcpyFromSymbol(&v, lean_error_word, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+    if (clear && v) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(lean_error_word, &zero, sizeof(zero)) != cudaSuccess)
+            return 0xFFFFFFFFu;
+    }
+    return v;
 }
 
 }  // extern "C"

@@ -6,20 +6,9 @@
 // nibbles per byte + f16 scale per 32; Q8: 32 weights per scale);
 // "wgpu-llm" README, INT8 mode (block 64); "lean" README model table (Q6_K).
 //
-// Packed side, per format (one row n; vector = 16 bytes):
-//   Q4_0   vector c = block c; word t bits 4i..4i+3 = q of block element 8t+i.
-//   Q8_0   vectors 2c, 2c+1 = block c; byte i = (q of element 16*(j%2)+i) + 128.
-//   I8_B64 vectors 4c..4c+3 = block c; byte i of vector 4c+j = element 16j+i,
-//          biased by 128.
-//   Q6_K   vectors 13s..13s+11 hold the 256 6-bit q of super-block s as 16
-//          sub-blocks of 3 words (48 words); vector 13s+12 holds the 16
-//          sub-scales, biased by 128.  Sub-block b (elements 16b..16b+15)
-//          occupies words 3b, 3b+1, 3b+2 =: W0, W1, W2, with local element
-//          i = 0..14 in word i/5 at bit 6*(i%5) and element 15 split into
-//          2-bit pieces: bits 0-1 in W2[30:31], bits 2-3 in W1[30:31],
-//          bits 4-5 in W0[30:31].
-//   Scales: fp16 bits copied as they are; Q4_0/Q8_0/I8_B64 one per block,
-//   Q6_K one d per super-block, 8 per scale vector.
+// Packed side: see layout.h (row groups of 32, steps of 8 blocks, quant
+// vectors then one scale vector per step).  Scales are fp16 bits copied as
+// they are; int8 values and Q6_K sub-scales are stored biased by 128.
 #include <cstring>
 
 #include "../../include/lean_qmatmul.h"
@@ -68,28 +57,29 @@ template <bool TO_PACKED>
 lean_status convert(int fmt, const uint8_t *canon, uint8_t *packed, int64_t N, int64_t K) {
     Geom g;
     if (!make_geom(fmt, N, K, &g)) return LEAN_ERR_SHAPE;
-    const int be = block_elems(fmt);
     const int64_t bb = block_bytes(fmt);
-    const int64_t nblk = K / be;
+    const int64_t nblk = g.blocks;
+    const int vpb = g.vpb;
     if (TO_PACKED) std::memset(packed, 0, (size_t)g.total);
-    uint8_t *qp = packed;
-    uint8_t *sp = packed + g.s_off;
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t c = 0; c < nblk; ++c) {
             const int64_t coff = (n * nblk + c) * bb;
-            // scale slot: blocks (Q4_0/Q8_0/I8) or super-blocks (Q6_K), 8 per vector
-            uint8_t *sv = sp + vec_offset(n, c / 8, g.svec) + 2 * (c % 8);
+            const int64_t s = c / kBlocksPerStep;
+            const int i = (int)(c % kBlocksPerStep);
+            // the step's scale vector follows its quant vectors; halfword i is block i's d
+            uint8_t *sv = packed + vec_offset(g, n, s, (int64_t)step_blocks(g, s) * vpb) + 2 * i;
+            auto qv = [&](int j) { return packed + vec_offset(g, n, s, (int64_t)i * vpb + j); };
             if (fmt == Q4_0) {
-                uint8_t *v = qp + vec_offset(n, c, g.qvec);
+                uint8_t *v = qv(0);
                 if (TO_PACKED) {
                     const uint8_t *b = canon + coff;
                     wr16(sv, rd16(b));
                     for (int t = 0; t < 4; ++t) {
                         uint32_t w = 0;
-                        for (int i = 0; i < 8; ++i) {
-                            int e = 8 * t + i;
+                        for (int k = 0; k < 8; ++k) {
+                            int e = 8 * t + k;
                             int q = e < 16 ? (b[2 + e] & 0xf) : (b[2 + e - 16] >> 4);
-                            w |= (uint32_t)q << (4 * i);
+                            w |= (uint32_t)q << (4 * k);
                         }
                         wr32(v + 4 * t, w);
                     }
@@ -99,28 +89,27 @@ lean_status convert(int fmt, const uint8_t *canon, uint8_t *packed, int64_t N, i
                     std::memset(b + 2, 0, 16);
                     for (int t = 0; t < 4; ++t) {
                         uint32_t w = rd32(v + 4 * t);
-                        for (int i = 0; i < 8; ++i) {
-                            int e = 8 * t + i, q = (w >> (4 * i)) & 0xf;
+                        for (int k = 0; k < 8; ++k) {
+                            int e = 8 * t + k, q = (w >> (4 * k)) & 0xf;
                             if (e < 16) b[2 + e] |= (uint8_t)q;
                             else b[2 + e - 16] |= (uint8_t)(q << 4);
                         }
                     }
                 }
             } else if (fmt == Q8_0 || fmt == I8_B64) {
-                const int nv = be / 16;  // vectors per block
                 if (TO_PACKED) {
                     const uint8_t *b = canon + coff;
                     wr16(sv, rd16(b));
-                    for (int j = 0; j < nv; ++j) {
-                        uint8_t *v = qp + vec_offset(n, c * nv + j, g.qvec);
-                        for (int i = 0; i < 16; ++i) v[i] = (uint8_t)(b[2 + 16 * j + i] ^ 0x80);
+                    for (int j = 0; j < vpb; ++j) {
+                        uint8_t *v = qv(j);
+                        for (int k = 0; k < 16; ++k) v[k] = (uint8_t)(b[2 + 16 * j + k] ^ 0x80);
                     }
                 } else {
                     uint8_t *b = const_cast<uint8_t *>(canon) + coff;
                     wr16(b, rd16(sv));
-                    for (int j = 0; j < nv; ++j) {
-                        const uint8_t *v = qp + vec_offset(n, c * nv + j, g.qvec);
-                        for (int i = 0; i < 16; ++i) b[2 + 16 * j + i] = (uint8_t)(v[i] ^ 0x80);
+                    for (int j = 0; j < vpb; ++j) {
+                        const uint8_t *v = qv(j);
+                        for (int k = 0; k < 16; ++k) b[2 + 16 * j + k] = (uint8_t)(v[k] ^ 0x80);
                     }
                 }
             } else {  // Q6_K
@@ -128,29 +117,27 @@ lean_status convert(int fmt, const uint8_t *canon, uint8_t *packed, int64_t N, i
                 if (TO_PACKED) {
                     const uint8_t *b = canon + coff;
                     wr16(sv, rd16(b + 208));
-                    for (int s = 0; s < 16; ++s) {
+                    for (int sb = 0; sb < 16; ++sb) {
                         int q[16];
                         uint32_t w[3];
-                        for (int i = 0; i < 16; ++i) q[i] = q6k_get(b, 16 * s + i);
+                        for (int k = 0; k < 16; ++k) q[k] = q6k_get(b, 16 * sb + k);
                         q6_words_from(q, w);
-                        for (int k = 0; k < 3; ++k) wr32(words + 4 * (3 * s + k), w[k]);
-                        words[192 + s] = (uint8_t)(b[192 + s] ^ 0x80);
+                        for (int k = 0; k < 3; ++k) wr32(words + 4 * (3 * sb + k), w[k]);
+                        words[192 + sb] = (uint8_t)(b[192 + sb] ^ 0x80);
                     }
-                    for (int j = 0; j < 13; ++j)
-                        std::memcpy(qp + vec_offset(n, c * 13 + j, g.qvec), words + 16 * j, 16);
+                    for (int j = 0; j < 13; ++j) std::memcpy(qv(j), words + 16 * j, 16);
                 } else {
                     uint8_t *b = const_cast<uint8_t *>(canon) + coff;
                     std::memset(b, 0, 210);
                     wr16(b + 208, rd16(sv));
-                    for (int j = 0; j < 13; ++j)
-                        std::memcpy(words + 16 * j, qp + vec_offset(n, c * 13 + j, g.qvec), 16);
-                    for (int s = 0; s < 16; ++s) {
+                    for (int j = 0; j < 13; ++j) std::memcpy(words + 16 * j, qv(j), 16);
+                    for (int sb = 0; sb < 16; ++sb) {
                         int q[16];
                         uint32_t w[3];
-                        for (int k = 0; k < 3; ++k) w[k] = rd32(words + 4 * (3 * s + k));
+                        for (int k = 0; k < 3; ++k) w[k] = rd32(words + 4 * (3 * sb + k));
                         q6_words_to(w, q);
-                        for (int i = 0; i < 16; ++i) q6k_put(b, 16 * s + i, q[i]);
-                        b[192 + s] = (uint8_t)(words[192 + s] ^ 0x80);
+                        for (int k = 0; k < 16; ++k) q6k_put(b, 16 * sb + k, q[k]);
+                        b[192 + sb] = (uint8_t)(words[192 + sb] ^ 0x80);
                     }
                 }
             }

@@ -1,8 +1,6 @@
-// qmm_i8_b64.cu -- I8_B64 instantiation of the CUDA-core product and dequant kernels.
-#include "simt_launch.cuh"
+// qmm_i8_b64.cu -- I8_B64 instantiation of the product and dequantisation kernels.
+#include "launch.cuh"
 
 namespace lean {
-template lean_status qmm_fmt<I8_B64>(const Geom &, const uint8_t *, const float *, float *, int64_t,
-                                 unsigned, cudaStream_t);
-template lean_status dequant_fmt<I8_B64>(const Geom &, const uint8_t *, float *, cudaStream_t);
+LEAN_INSTANTIATE(I8_B64)
 }  // namespace lean

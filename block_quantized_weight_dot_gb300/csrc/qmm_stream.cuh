@@ -1,0 +1,419 @@
+// qmm_stream.cuh -- the decode GEMV (M = 1) as a TMA-fed streaming kernel.
+//
+// Decode streams every weight once ("oxinfer" crate page, Performance: decode
+// is memory-bandwidth bound, each generated token streams all dense weights
+// once), so this kernel is a pipeline whose only job is to keep HBM busy:
+//
+//  - one producer lane per CTA copies whole steps (8 blocks of one 32-row
+//    group: their quant vectors and scale vector, contiguous in the packed
+//    layout) plus the matching slice of x into a ring of shared-memory slots
+//    with bulk asynchronous copies (cp.async.bulk, completion counted in bytes
+//    on an mbarrier per slot);
+//  - eight consumer warps decode the slot from shared memory (lane r owns row
+//    r of the group: conflict-free 16-byte reads; x is a broadcast read) and
+//    accumulate in fp32, then release the slot on a second mbarrier;
+//  - a CTA works on a contiguous range of the flattened (problem, row group,
+//    step) list.  Without a workspace the ranges are whole row groups; with a
+//    workspace they are equal numbers of steps (stream-K), and a group split
+//    between CTAs is completed by the last CTA to arrive, which adds the
+//    parts in CTA order: results are deterministic either way;
+//  - weights are requested before griddepcontrol.wait, x after it, so with
+//    programmatic dependent launch the weight stream of one product overlaps
+//    the tail of the previous kernel on the stream;
+//  - every wait is bounded (globaltimer); on timeout the kernel records an
+//    error code, lets its own copies land and returns.
+//
+// Several independent products (same format, M = 1) can share one launch: the
+// list of problems is a kernel parameter, and their steps are concatenated.
+#pragma once
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "decode.cuh"
+#include "layout.h"
+#include "ptx.cuh"
+
+namespace lean {
+
+constexpr int kStreamWarps = 8;                          // consumer warps per CTA
+constexpr int kStreamThreads = 32 * (kStreamWarps + 1);  // + one producer warp
+constexpr uint64_t kWaitLimitNs = 2000000000ull;        // 2 s
+
+enum StreamError : unsigned {
+    kErrFullTimeout = 1u,   // a consumer waited too long for a slot
+    kErrEmptyTimeout = 2u,  // the producer waited too long for a free slot
+};
+
+struct StreamProb {
+    const uint8_t *W;
+    const float *x;
+    float *y;
+    int N, K;
+    int steps, last_blocks;  // steps per group, blocks in a group's last step
+    int64_t group_vecs;      // vectors per row group
+    int64_t groups;          // row groups
+    int64_t step0, group0;   // first global step / group of this problem
+};
+
+template <int NP>
+struct StreamArgs {
+    int nprob;
+    int ctas;
+    int balanced;  // 1: equal steps per CTA (needs part/cnt); 0: whole groups per CTA
+    int64_t total_steps, total_groups;
+    float *part;    // [ctas][2][32] partial sums of groups split between CTAs
+    unsigned *cnt;  // [total_groups] arrival counters, all zero between calls
+    unsigned *err;  // device error word (bits of StreamError)
+    Magic mg;
+    StreamProb p[NP];
+};
+
+template <int FMT> struct StreamCfg;
+// VPB: quant vectors per block; SE: x elements per step; KS: steps per slot;
+// S: slots in the ring.  A slot is about 20-60 KB; the ring about 150-190 KB.
+template <> struct StreamCfg<Q4_0> { static constexpr int VPB = 1, SE = 256, KS = 4, S = 6; };
+template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, SE = 256, KS = 4, S = 4; };
+template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, SE = 512, KS = 2, S = 4; };
+template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, SE = 2048, KS = 1, S = 3; };
+
+template <int FMT>
+struct StreamLayout {
+    using C = StreamCfg<FMT>;
+    static constexpr int STEP_WBYTES = (8 * C::VPB + 1) * kVecBytes;
+    static constexpr int STEP_XBYTES = C::SE * 4;
+    static constexpr int STEP_BYTES = STEP_WBYTES + STEP_XBYTES;
+    static constexpr int SLOT_BYTES = C::KS * STEP_BYTES;
+    static constexpr int WPS = kStreamWarps / C::KS;  // warps per step
+    static constexpr int BPW = 8 / WPS;               // blocks per warp
+    static constexpr int R = (C::S + 1) * C::KS + 3;  // ring of groups being reduced
+    // shared memory: [full S][empty S][cnt R][red R*W*32][pad][ring S*SLOT]
+    static constexpr int OFF_FULL = 0;
+    static constexpr int OFF_EMPTY = 8 * C::S;
+    static constexpr int OFF_CNT = 16 * C::S;
+    static constexpr int OFF_RED = OFF_CNT + 4 * R;
+    static constexpr int OFF_RING = ((OFF_RED + 4 * R * kStreamWarps * 32) + 127) / 128 * 128;
+    static constexpr int SMEM = OFF_RING + C::S * SLOT_BYTES;
+};
+
+__device__ __forceinline__ int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ int64_t i64max(int64_t a, int64_t b) { return a > b ? a : b; }
+
+template <int NP>
+__device__ __forceinline__ int find_prob_by_step(const StreamArgs<NP> &a, int64_t t) {
+    int lo = 0, hi = a.nprob - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.p[mid].step0 <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+template <int NP>
+__device__ __forceinline__ int find_prob_by_group(const StreamArgs<NP> &a, int64_t g) {
+    int lo = 0, hi = a.nprob - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.p[mid].group0 <= g) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+// first global step of global group g (g == total_groups gives total_steps)
+template <int NP>
+__device__ __forceinline__ int64_t group_first_step(const StreamArgs<NP> &a, int64_t g) {
+    if (g >= a.total_groups) return a.total_steps;
+    const StreamProb &p = a.p[find_prob_by_group(a, g)];
+    return p.step0 + (g - p.group0) * p.steps;
+}
+template <int NP>
+__device__ __forceinline__ int64_t range_begin(const StreamArgs<NP> &a, int64_t i) {
+    if (a.balanced) return a.total_steps * i / a.ctas;
+    return group_first_step(a, a.total_groups * i / a.ctas);
+}
+// the CTA whose balanced range holds step t
+template <int NP>
+__device__ __forceinline__ int64_t cta_of_step(const StreamArgs<NP> &a, int64_t t) {
+    int64_t i = t * a.ctas / a.total_steps;
+    while (i + 1 < a.ctas && a.total_steps * (i + 1) / a.ctas <= t) ++i;
+    while (i > 0 && a.total_steps * i / a.ctas > t) --i;
+    return i;
+}
+
+// ---- per-format consumer work on one step held in shared memory -------------
+// Returns this warp's share of sum_k w x for its lane's row, blocks [b0, b0+BPW).
+template <int FMT>
+__device__ __forceinline__ float consume_step(const uint8_t *ws, const float *xs, int nblk, int b0,
+                                              int lane, const Magic &mg) {
+    using C = StreamCfg<FMT>;
+    constexpr int BPW = StreamLayout<FMT>::BPW;
+    const uint4 sv = *reinterpret_cast<const uint4 *>(ws + nblk * C::VPB * kVecBytes + lane * 16);
+    float acc = 0.f;
+    if (FMT == Q4_0) {
+#pragma unroll
+        for (int i = 0; i < BPW; ++i) {
+            const int b = b0 + i;
+            if (b < nblk) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(ws + b * kVecBytes + lane * 16);
+                const float *xb = xs + b * 32;
+                f32x2 s = 0ull;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    f32x2 p[4];
+                    q4_word(word_of(v, t), mg, p);
+                    const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t);
+                    const ulonglong2 xc = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t + 4);
+                    s = fma2(p[0], xa.x, s);
+                    s = fma2(p[1], xa.y, s);
+                    s = fma2(p[2], xc.x, s);
+                    s = fma2(p[3], xc.y, s);
+                }
+                const float2 r = unpack2(s);
+                acc = fmaf(scale_of(sv, b), r.x + r.y, acc);
+            }
+        }
+    } else if (FMT == Q8_0 || FMT == I8_B64) {
+#pragma unroll
+        for (int i = 0; i < BPW; ++i) {
+            const int b = b0 + i;
+            if (b < nblk) {
+                f32x2 s = 0ull;
+#pragma unroll
+                for (int j = 0; j < C::VPB; ++j) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        ws + (b * C::VPB + j) * kVecBytes + lane * 16);
+                    const float *xb = xs + (b * C::VPB + j) * 16;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        f32x2 p[2];
+                        i8_word(word_of(v, t), mg, p);
+                        const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xb + 4 * t);
+                        s = fma2(p[0], xa.x, s);
+                        s = fma2(p[1], xa.y, s);
+                    }
+                }
+                const float2 r = unpack2(s);
+                acc = fmaf(scale_of(sv, b), r.x + r.y, acc);
+            }
+        }
+    } else {  // Q6_K: one super-block per warp, 16 sub-blocks with int8 sub-scales
+#pragma unroll
+        for (int i = 0; i < BPW; ++i) {
+            const int b = b0 + i;
+            if (b < nblk) {
+                const uint8_t *sb = ws + b * C::VPB * kVecBytes + lane * 16;
+                const float d = scale_of(sv, b);
+                const uint4 scv = *reinterpret_cast<const uint4 *>(sb + 12 * kVecBytes);
+                const float *xb = xs + b * 256;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {  // 4 sub-blocks per 3 vectors
+                    const uint4 v0 = *reinterpret_cast<const uint4 *>(sb + (3 * q + 0) * kVecBytes);
+                    const uint4 v1 = *reinterpret_cast<const uint4 *>(sb + (3 * q + 1) * kVecBytes);
+                    const uint4 v2 = *reinterpret_cast<const uint4 *>(sb + (3 * q + 2) * kVecBytes);
+                    const uint32_t w[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y,
+                                            v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int sub = 4 * q + u;
+                        f32x2 p[8];
+                        q6_group(w[3 * u], w[3 * u + 1], w[3 * u + 2], mg, p);
+                        f32x2 s = 0ull;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const ulonglong2 xa =
+                                *reinterpret_cast<const ulonglong2 *>(xb + sub * 16 + 4 * j);
+                            s = fma2(p[2 * j], xa.x, s);
+                            s = fma2(p[2 * j + 1], xa.y, s);
+                        }
+                        const float sc = i8_byte(word_of(scv, sub >> 2), sub & 3, mg);
+                        const float2 r = unpack2(s);
+                        acc = fmaf(d * sc, r.x + r.y, acc);
+                    }
+                }
+            }
+        }
+    }
+    return acc;
+}
+
+template <int FMT, int NP>
+__global__ void __launch_bounds__(kStreamThreads, 1) qmm_stream_kernel(const __grid_constant__ StreamArgs<NP> a) {
+    using C = StreamCfg<FMT>;
+    using L = StreamLayout<FMT>;
+    extern __shared__ __align__(128) uint8_t sbuf[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(sbuf + L::OFF_FULL);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(sbuf + L::OFF_EMPTY);
+    unsigned *gcnt = reinterpret_cast<unsigned *>(sbuf + L::OFF_CNT);
+    float *red = reinterpret_cast<float *>(sbuf + L::OFF_RED);
+    uint8_t *ring = sbuf + L::OFF_RING;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t cta = blockIdx.x;
+    const int64_t beg = range_begin(a, cta), end = range_begin(a, cta + 1);
+    const int64_t nsteps = end - beg;
+    const int64_t nslots = (nsteps + C::KS - 1) / C::KS;
+
+    // Let the next kernel on the stream start streaming its own weights.
+    pdl_launch_dependents();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kStreamWarps);
+        }
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < L::R; i += blockDim.x) gcnt[i] = 0;
+    for (int i = threadIdx.x; i < L::R * kStreamWarps * 32; i += blockDim.x) red[i] = 0.f;
+    __syncthreads();
+    if (nsteps <= 0) return;
+
+    if (warp == kStreamWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        auto slot_steps = [&](int64_t j) {
+            return (int)i64min(C::KS, nsteps - j * C::KS);
+        };
+        // arm slot j and copy its weights (and x when x_ok)
+        auto issue = [&](int64_t j, bool weights, bool xs) {
+            const int sl = (int)(j % C::S);
+            uint8_t *base = ring + sl * L::SLOT_BYTES;
+            const int ns = slot_steps(j);
+            if (weights) {
+                uint32_t bytes = 0;
+                for (int i = 0; i < ns; ++i) {
+                    const int64_t t = beg + j * C::KS + i;
+                    const StreamProb &p = a.p[find_prob_by_step(a, t)];
+                    const int64_t o = t - p.step0;
+                    const int s = (int)(o % p.steps);
+                    const int nblk = s == p.steps - 1 ? p.last_blocks : 8;
+                    bytes += (nblk * C::VPB + 1) * kVecBytes;
+                    const int xe = min(C::SE, p.K - s * C::SE);
+                    bytes += xe * 4;
+                }
+                mbar_arrive_expect_tx(&full[sl], bytes);
+            }
+            for (int i = 0; i < ns; ++i) {
+                const int64_t t = beg + j * C::KS + i;
+                const StreamProb &p = a.p[find_prob_by_step(a, t)];
+                const int64_t o = t - p.step0;
+                const int64_t g = o / p.steps;
+                const int s = (int)(o % p.steps);
+                const int nblk = s == p.steps - 1 ? p.last_blocks : 8;
+                uint8_t *dst = base + i * L::STEP_BYTES;
+                if (weights) {
+                    const uint8_t *src =
+                        p.W + (g * p.group_vecs + (int64_t)s * (8 * C::VPB + 1)) * kVecBytes;
+                    bulk_g2s(dst, src, (nblk * C::VPB + 1) * kVecBytes, &full[sl]);
+                }
+                if (xs) {
+                    const int xe = min(C::SE, p.K - s * C::SE);
+                    bulk_g2s(dst + L::STEP_WBYTES, p.x + (int64_t)s * C::SE, xe * 4, &full[sl]);
+                }
+            }
+        };
+        const int64_t nfill = i64min(C::S, nslots);
+        for (int64_t j = 0; j < nfill; ++j) issue(j, true, false);
+        pdl_wait();  // x may be written by the previous kernel on the stream
+        for (int64_t j = 0; j < nfill; ++j) issue(j, false, true);
+        for (int64_t j = nfill; j < nslots; ++j) {
+            const int sl = (int)(j % C::S);
+            if (!mbar_wait(&empty[sl], (uint32_t)((j / C::S - 1) & 1), kWaitLimitNs)) {
+                atomicOr(a.err, kErrEmptyTimeout);
+                // let the copies already issued land before the CTA can exit
+                for (int64_t k = i64max(0, j - C::S); k < j; ++k)
+                    mbar_wait(&full[k % C::S], (uint32_t)((k / C::S) & 1), kWaitLimitNs);
+                return;
+            }
+            issue(j, true, true);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int si = warp / L::WPS;            // step of the slot this warp works on
+    const int b0 = (warp % L::WPS) * L::BPW;  // its first block in that step
+    const int64_t gfirst = [&] {
+        const StreamProb &p = a.p[find_prob_by_step(a, beg)];
+        return p.group0 + (beg - p.step0) / p.steps;
+    }();
+    float acc = 0.f;
+    int64_t cur = -1;  // global group being accumulated
+
+    // hand this warp's sum for group g to the CTA; the last contributor
+    // completes the group
+    auto deposit = [&](int64_t g, float v) {
+        const int r = (int)((g - gfirst) % L::R);
+        red[(r * kStreamWarps + warp) * 32 + lane] = v;
+        __threadfence_block();
+        __syncwarp();
+        unsigned old = 0;
+        if (lane == 0) old = atomicAdd(&gcnt[r], 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        // CTA-local steps of g and the warps that touch them
+        const StreamProb &p = a.p[find_prob_by_group(a, g)];
+        const int64_t gs = p.step0 + (g - p.group0) * p.steps, ge = gs + p.steps;
+        const int64_t ls = i64max(gs, beg), le = i64min(ge, end);
+        const unsigned expect = (unsigned)(i64min(le - ls, C::KS) * L::WPS);
+        if (old + 1 != expect) return;
+        __threadfence_block();
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kStreamWarps; ++w) {
+            s += red[(r * kStreamWarps + w) * 32 + lane];
+            red[(r * kStreamWarps + w) * 32 + lane] = 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) gcnt[r] = 0;
+        const int64_t n = (g - p.group0) * kRowsPerGroup + lane;
+        if (gs >= beg && ge <= end) {  // the whole group is in this CTA
+            if (n < p.N) p.y[n] = s;
+            return;
+        }
+        // group split between CTAs (balanced ranges): publish, the last CTA adds up
+        const int side = gs < beg ? 0 : 1;
+        a.part[(cta * 2 + side) * 32 + lane] = s;
+        __threadfence();
+        __syncwarp();
+        unsigned arrived = 0;
+        if (lane == 0) arrived = atomicAdd(&a.cnt[g], 1u);
+        arrived = __shfl_sync(0xffffffffu, arrived, 0);
+        const int64_t i0 = cta_of_step(a, gs), i1 = cta_of_step(a, ge - 1);
+        if (arrived + 1 != (unsigned)(i1 - i0 + 1)) return;
+        __threadfence();
+        float tot = 0.f;
+        for (int64_t i = i0; i <= i1; ++i) {
+            const int sd = (i == i0) ? 1 : 0;
+            tot += __ldcg(&a.part[(i * 2 + sd) * 32 + lane]);
+        }
+        if (n < p.N) p.y[n] = tot;
+        if (lane == 0) a.cnt[g] = 0;  // ready for the next call
+    };
+
+    for (int64_t j = 0; j < nslots; ++j) {
+        const int sl = (int)(j % C::S);
+        if (!mbar_wait(&full[sl], (uint32_t)((j / C::S) & 1), kWaitLimitNs)) {
+            if (lane == 0) atomicOr(a.err, kErrFullTimeout);
+            return;
+        }
+        const int64_t l = j * C::KS + si;
+        if (l < nsteps) {
+            const int64_t t = beg + l;
+            const StreamProb &p = a.p[find_prob_by_step(a, t)];
+            const int64_t o = t - p.step0;
+            const int64_t g = p.group0 + o / p.steps;
+            const int s = (int)(o % p.steps);
+            const int nblk = s == p.steps - 1 ? p.last_blocks : 8;
+            if (g != cur) {
+                if (cur >= 0) deposit(cur, acc);
+                cur = g;
+                acc = 0.f;
+            }
+            const uint8_t *ws = ring + sl * L::SLOT_BYTES + si * L::STEP_BYTES;
+            const float *xs = reinterpret_cast<const float *>(ws + L::STEP_WBYTES);
+            acc += consume_step<FMT>(ws, xs, nblk, b0, lane, a.mg);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[sl]);
+    }
+    if (cur >= 0) deposit(cur, acc);
+}
+
+}  // namespace lean

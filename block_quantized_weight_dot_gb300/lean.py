@@ -32,8 +32,21 @@ SIGNATURES = {
     "lean_dequant": (_int, [_int, _vp, _vp, _i64, _i64, _vp]),
     "lean_qmatmul": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "lean_qmatmul_ex": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp]),
+    "lean_qmatmul_workspace_bytes": (_i64, [_int, _i64, _i64, _i64]),
+    "lean_qmatmul_ws": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp, _i64,
+                               _vp]),
+    "lean_batch_workspace_bytes": (_i64, [_int, _int, _vp]),
+    "lean_qmatmul_batch": (_int, [_int, _int, _vp, ctypes.c_uint, _vp, _i64, _vp]),
+    "lean_device_error": (ctypes.c_uint, [_int]),
     "lean_status_str": (ctypes.c_char_p, [_int]),
 }
+LEAN_MAX_BATCH = 256
+
+
+class lean_problem(ctypes.Structure):
+    """One product of a batch: device pointers and its shape (C struct lean_problem)."""
+    _fields_ = [("W", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 class LeanError(RuntimeError):
@@ -153,6 +166,46 @@ def lean_qmatmul_ex(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int
     """lean_qmatmul with launch flags (LEAN_FLAG_EARLY_WEIGHTS)."""
     _check("lean_qmatmul_ex", _lib.lean_qmatmul_ex(fmt, _addr(W_packed_dev), _addr(x_dev),
                                                    _addr(y_dev), N, K, M, flags, _stream(stream)))
+
+
+def lean_qmatmul_workspace_bytes(fmt: int, N: int, K: int, M: int) -> int:
+    return _lib.lean_qmatmul_workspace_bytes(fmt, N, K, M)
+
+
+def lean_qmatmul_ws(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,
+                    flags: int = 0, workspace=None, workspace_bytes: int = 0,
+                    stream=None) -> None:
+    """lean_qmatmul with flags and a caller-owned, once-zeroed device workspace."""
+    _check("lean_qmatmul_ws", _lib.lean_qmatmul_ws(fmt, _addr(W_packed_dev), _addr(x_dev),
+                                                   _addr(y_dev), N, K, M, flags,
+                                                   _addr(workspace), workspace_bytes,
+                                                   _stream(stream)))
+
+
+def make_problems(items):
+    """ctypes array of lean_problem from (W, x, y, N, K) tuples."""
+    arr = (lean_problem * len(items))()
+    for i, (W, x, y, N, K) in enumerate(items):
+        arr[i] = lean_problem(_addr(W), _addr(x), _addr(y), N, K)
+    return arr
+
+
+def lean_batch_workspace_bytes(fmt: int, problems) -> int:
+    return _lib.lean_batch_workspace_bytes(fmt, len(problems), ctypes.cast(problems, _vp))
+
+
+def lean_qmatmul_batch(fmt: int, problems, flags: int = 0, workspace=None,
+                       workspace_bytes: int = 0, stream=None) -> None:
+    """Independent M = 1 products in one launch; `problems` from make_problems()."""
+    _check("lean_qmatmul_batch", _lib.lean_qmatmul_batch(fmt, len(problems),
+                                                         ctypes.cast(problems, _vp), flags,
+                                                         _addr(workspace), workspace_bytes,
+                                                         _stream(stream)))
+
+
+def lean_device_error(clear: bool = True) -> int:
+    """Device error word (non-zero: a kernel's bounded wait timed out)."""
+    return _lib.lean_device_error(1 if clear else 0)
 
 
 # ---- torch conveniences (device memory via PyTorch; compute via the library) ----

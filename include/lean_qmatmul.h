@@ -147,6 +147,57 @@ lean_status lean_qmatmul_ex(int fmt, const void *W_packed_dev, const float *x_de
                             float *y_dev, int64_t N, int64_t K, int64_t M,
                             unsigned flags, void *stream);
 
+/* Bytes of device workspace that lean_qmatmul_ws uses for this shape (0 when
+ * the shape needs none: M > 1), or -1 on a bad fmt or shape. */
+int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);
+
+/* lean_qmatmul_ex with a caller-owned device workspace.  With a workspace the
+ * M = 1 product splits K-steps evenly over all SMs, also inside a 32-row
+ * group, and the CTA that finishes a split group last adds the parts up (in
+ * a fixed order, so results stay deterministic); without one (NULL) every
+ * CTA owns whole row groups, which balances well only when N/32 is much
+ * larger than the SM count.
+ *   workspace        device, 256-byte aligned, >= lean_qmatmul_workspace_bytes
+ *                    bytes; it must be zeroed once (cudaMemset) before its
+ *                    first use, and every call leaves it zeroed again.
+ *   workspace_bytes  its size (LEAN_ERR_SHAPE if too small).
+ * Calls that may run at the same time on the GPU must not share a workspace.
+ * The workspace is ignored for M > 1. */
+lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_dev,
+                            float *y_dev, int64_t N, int64_t K, int64_t M,
+                            unsigned flags, void *workspace, int64_t workspace_bytes,
+                            void *stream);
+
+/* Several independent M = 1 products of one format in a single launch, for a
+ * decode step whose linears do not depend on each other (or one dependency
+ * level of a layer, e.g. q/k/v or gate/up).  Their row-group steps are
+ * concatenated and streamed by one persistent grid. */
+#define LEAN_MAX_BATCH 256
+typedef struct {
+    const void *W;  /* device, packed by lean_pack, 16-byte aligned         */
+    const float *x; /* device, x[K] fp32, 16-byte aligned                   */
+    float *y;       /* device, y[N] fp32, overwritten                       */
+    int64_t N, K;
+} lean_problem;
+
+/* Workspace bytes for lean_qmatmul_batch over these problems, or -1. */
+int64_t lean_batch_workspace_bytes(int fmt, int count, const lean_problem *problems);
+
+/* problems: host array of `count` (1..LEAN_MAX_BATCH) descriptors, read during
+ * the call only.  workspace / workspace_bytes / flags as for lean_qmatmul_ws
+ * (workspace may be NULL).  Outputs of different problems must not overlap
+ * each other or any input. */
+lean_status lean_qmatmul_batch(int fmt, int count, const lean_problem *problems,
+                               unsigned flags, void *workspace, int64_t workspace_bytes,
+                               void *stream);
+
+/* The device error word of the current device: non-zero when a kernel gave up
+ * waiting on one of its own pipeline barriers (a bounded wait timed out and
+ * the kernel returned early; its outputs are then invalid).  Reads it
+ * synchronously (the device is synchronised first) and clears it when
+ * `clear` is non-zero.  Returns 0xFFFFFFFF if the word cannot be read. */
+unsigned lean_device_error(int clear);
+
 /* Static description of a status code. */
 const char *lean_status_str(int status);
 

@@ -203,3 +203,97 @@ def test_flags_rejected(lean):
     st = torch.cuda.current_stream().cuda_stream
     assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, 2,
                                      st) == lean.LEAN_ERR_FORMAT
+
+
+# ---- workspace (stream-K split of row groups) and batched launches -------------
+
+WS_SHAPES = [(1, 1), (33, 3), (64, 43), (100, 17), (32, 200), (65, 9)]
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+@pytest.mark.parametrize("N,nblk", WS_SHAPES)
+def test_workspace_split_groups(lean, fmt, N, nblk):
+    """M = 1 with a workspace: row groups split between CTAs are completed by
+    the last CTA; two calls in a row (the workspace must come back zeroed)."""
+    torch = torch_cuda()
+    be = syn.BLOCK_ELEMS[fmt]
+    if fmt == syn.Q6_K:
+        nblk = max(1, nblk // 3)
+    K = nblk * be
+    W, x = syn.make_problem(fmt, N, K, 1, seed=(29, fmt, N, K))
+    Wd = lean.upload_packed(fmt, W, N, K)
+    xd = torch.from_numpy(x).cuda()
+    nb = lean.lean_qmatmul_workspace_bytes(fmt, N, K, 1)
+    assert nb > 0
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    y_ref, bound = oracle.qmatmul(fmt, W, x, N, K)
+    outs = []
+    for _ in range(2):
+        yd = torch.full((1, N), float("nan"), device="cuda")
+        lean.lean_qmatmul_ws(fmt, Wd, xd, yd, N, K, 1, 0, ws, nb)
+        torch.cuda.synchronize()
+        y = yd.cpu().numpy().astype(np.float64)
+        check_close(y, y_ref, bound, "ws %s N=%d K=%d" % (syn.FORMAT_NAMES[fmt], N, K))
+        outs.append(y)
+    assert np.array_equal(outs[0], outs[1])
+    # the counters region must be back to zero
+    cnt_off = 256 * 2 * 32 * 4
+    assert int(ws[cnt_off:].count_nonzero()) == 0
+    assert lean.lean_device_error(True) == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+@pytest.mark.parametrize("use_ws", [False, True], ids=["whole_groups", "workspace"])
+def test_batch(lean, fmt, use_ws):
+    torch = torch_cuda()
+    be = syn.BLOCK_ELEMS[fmt]
+    shapes = [(1, 1), (40, 3), (960, 30), (33, 8), (320, 17), (64, 1), (100, 9)]
+    if fmt == syn.Q6_K:
+        shapes = [(N, max(1, n // 4)) for N, n in shapes]
+    items, keep, refs = [], [], []
+    for i, (N, nblk) in enumerate(shapes):
+        K = nblk * be
+        W, x = syn.make_problem(fmt, N, K, 1, seed=(30, fmt, i))
+        Wd = lean.upload_packed(fmt, W, N, K)
+        xd = torch.from_numpy(x).cuda()
+        yd = torch.full((N,), float("nan"), device="cuda")
+        keep += [Wd, xd, yd]
+        items.append((Wd, xd, yd, N, K))
+        refs.append(oracle.qmatmul(fmt, W, x, N, K))
+    probs = lean.make_problems(items)
+    ws, nb = None, 0
+    if use_ws:
+        nb = lean.lean_batch_workspace_bytes(fmt, probs)
+        ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for it in items:
+            it[2].fill_(float("nan"))
+        lean.lean_qmatmul_batch(fmt, probs, lean.LEAN_FLAG_EARLY_WEIGHTS, ws, nb)
+        torch.cuda.synchronize()
+        for (Wd, xd, yd, N, K), (y_ref, bound) in zip(items, refs):
+            check_close(yd.cpu().numpy().astype(np.float64)[None, :], y_ref, bound,
+                        "batch N=%d K=%d" % (N, K))
+    assert lean.lean_device_error(True) == 0
+
+
+def test_batch_argument_errors(lean):
+    torch = torch_cuda()
+    W, x = syn.make_problem(syn.Q4_0, 32, 64, 1, seed=(31,))
+    Wd = lean.upload_packed(syn.Q4_0, W, 32, 64)
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty(32, device="cuda")
+    good = lean.make_problems([(Wd, xd, yd, 32, 64)])
+    f = lean._lib.lean_qmatmul_batch
+    st = torch.cuda.current_stream().cuda_stream
+    import ctypes
+    p = ctypes.cast(good, ctypes.c_void_p)
+    assert f(0, 0, p, 0, None, 0, st) == lean.LEAN_ERR_SHAPE
+    assert f(0, 257, p, 0, None, 0, st) == lean.LEAN_ERR_SHAPE
+    assert f(0, 1, None, 0, None, 0, st) == lean.LEAN_ERR_NULL
+    assert f(9, 1, p, 0, None, 0, st) == lean.LEAN_ERR_FORMAT
+    bad = lean.make_problems([(Wd, xd, yd, 32, 48)])
+    assert f(0, 1, ctypes.cast(bad, ctypes.c_void_p), 0, None, 0, st) == lean.LEAN_ERR_SHAPE
+    ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    assert f(0, 1, p, 0, ws.data_ptr(), 64, st) == lean.LEAN_ERR_SHAPE  # too small
+    assert f(0, 1, p, 0, None, 0, st) == lean.LEAN_OK
+    torch.cuda.synchronize()
