@@ -71,13 +71,14 @@ def test_pack_round_trip(lean, fmt):
 
 
 def test_pack_padding_is_zero(lean):
-    """Rows past N in the last 32-row group are written as zeros."""
-    fmt, N, K = 0, 33, 64
+    """Rows past N in the last 32-row group and unused scale slots are zeros."""
+    fmt, N, K = 0, 33, 64  # two blocks: one step of 2 quant vectors + 1 scale vector
     W = np.full(syn.canonical_bytes(fmt, N, K), 0xFF, np.uint8)
-    p = lean.lean_pack(fmt, W, N, K).reshape(-1)
-    # quant plane: group 1 holds row 32 only -> lanes 1..31 of its vectors are zero
-    q = p[:2 * 2 * 512].reshape(2, 2, 32, 16)
-    assert (q[1, :, 1:, :] == 0).all() and (q[1, :, 0, :] == 0xFF).all()
+    p = lean.lean_pack(fmt, W, N, K).reshape(2, 3, 32, 16)  # [group][vector][row][16 B]
+    assert (p[0, :2] == 0xFF).all()                 # group 0: every row present
+    assert (p[1, :, 1:, :] == 0).all()              # group 1: rows 33..63 are padding
+    assert (p[1, :2, 0, :] == 0xFF).all()           # row 32's quant vectors
+    assert (p[1, 2, 0, :4] == 0xFF).all() and (p[1, 2, 0, 4:] == 0).all()  # 2 of 8 scales
 
 
 def test_host_argument_errors(lean):
