@@ -143,7 +143,8 @@ lean_status launch_simt(const Geom &g, const uint8_t *W, const float *x, float *
     a.wpr = p.wpr;
     a.xs_stride = p.xs_stride;
     auto kern = qmm_simt_kernel<FMT, MT>;
-    if (!ensure_smem(kern, p.smem, smem_done)) return LEAN_ERR_CUDA;
+    // the attribute is set once per device, to the most any plan asks for
+    if (!ensure_smem(kern, kMaxSimtSmem, smem_done)) return LEAN_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.ctas, 1, 1);
     cfg.blockDim = dim3((unsigned)(32 * p.rg * p.wpr), 1, 1);

@@ -86,10 +86,11 @@ struct StreamLayout {
     static constexpr int WPS = kStreamWarps / C::KS;  // warps per step
     static constexpr int BPW = 8 / WPS;               // blocks per warp
     static constexpr int R = (C::S + 1) * C::KS + 3;  // ring of groups being reduced
-    // shared memory: [full S][empty S][cnt R][red R*W*32][pad][ring S*SLOT]
+    // shared memory: [full S][empty S][meta S*KS][cnt R][red R*W*32][pad][ring S*SLOT]
     static constexpr int OFF_FULL = 0;
     static constexpr int OFF_EMPTY = 8 * C::S;
-    static constexpr int OFF_CNT = 16 * C::S;
+    static constexpr int OFF_META = 16 * C::S;
+    static constexpr int OFF_CNT = OFF_META + 48 * C::S * C::KS;
     static constexpr int OFF_RED = OFF_CNT + 4 * R;
     static constexpr int OFF_RING = ((OFF_RED + 4 * R * kStreamWarps * 32) + 127) / 128 * 128;
     static constexpr int SMEM = OFF_RING + C::S * SLOT_BYTES;
@@ -233,15 +234,30 @@ __device__ __forceinline__ float consume_step(const uint8_t *ws, const float *xs
     return acc;
 }
 
+// What the producer learned about one step of a slot, for the consumers.
+struct StepMeta {
+    int64_t g;       // global row group
+    int64_t gs, ge;  // global step range of that group
+    const float *x;  // x slice copied for the step
+    int pi;          // problem index
+    int nblk;        // blocks in the step
+    int xe;          // x elements copied
+    int step;        // step inside the group
+};
+static_assert(sizeof(StepMeta) == 48, "StepMeta layout");
+
 template <int FMT, int NP>
-__global__ void __launch_bounds__(kStreamThreads, 1) qmm_stream_kernel(const __grid_constant__ StreamArgs<NP> a) {
+__global__ void __launch_bounds__(kStreamThreads, 1)
+    qmm_stream_kernel(const __grid_constant__ StreamArgs<NP> a) {
     using C = StreamCfg<FMT>;
     using L = StreamLayout<FMT>;
+    constexpr int SV = 8 * C::VPB + 1;  // vectors of a full step
     extern __shared__ __align__(128) uint8_t sbuf[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sbuf + L::OFF_FULL);
     uint64_t *empty = reinterpret_cast<uint64_t *>(sbuf + L::OFF_EMPTY);
     unsigned *gcnt = reinterpret_cast<unsigned *>(sbuf + L::OFF_CNT);
     float *red = reinterpret_cast<float *>(sbuf + L::OFF_RED);
+    StepMeta *meta = reinterpret_cast<StepMeta *>(sbuf + L::OFF_META);
     uint8_t *ring = sbuf + L::OFF_RING;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -268,51 +284,64 @@ __global__ void __launch_bounds__(kStreamThreads, 1) qmm_stream_kernel(const __g
     if (warp == kStreamWarps) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        auto slot_steps = [&](int64_t j) {
-            return (int)i64min(C::KS, nsteps - j * C::KS);
-        };
-        // arm slot j and copy its weights (and x when x_ok)
-        auto issue = [&](int64_t j, bool weights, bool xs) {
+        // cursor over the CTA's steps: problem, group inside it, step inside the group
+        int pi = find_prob_by_step(a, beg);
+        int64_t g, s;
+        {
+            const int64_t o = beg - a.p[pi].step0;
+            g = o / a.p[pi].steps;
+            s = o % a.p[pi].steps;
+        }
+        // fill the metadata of slot j and copy its weights; returns the bytes armed
+        auto issue_weights = [&](int64_t j) {
             const int sl = (int)(j % C::S);
+            const int ns = (int)i64min(C::KS, nsteps - j * C::KS);
             uint8_t *base = ring + sl * L::SLOT_BYTES;
-            const int ns = slot_steps(j);
-            if (weights) {
-                uint32_t bytes = 0;
-                for (int i = 0; i < ns; ++i) {
-                    const int64_t t = beg + j * C::KS + i;
-                    const StreamProb &p = a.p[find_prob_by_step(a, t)];
-                    const int64_t o = t - p.step0;
-                    const int s = (int)(o % p.steps);
-                    const int nblk = s == p.steps - 1 ? p.last_blocks : 8;
-                    bytes += (nblk * C::VPB + 1) * kVecBytes;
-                    const int xe = min(C::SE, p.K - s * C::SE);
-                    bytes += xe * 4;
-                }
-                mbar_arrive_expect_tx(&full[sl], bytes);
-            }
+            StepMeta *m = meta + sl * C::KS;
+            uint32_t bytes = 0;
             for (int i = 0; i < ns; ++i) {
-                const int64_t t = beg + j * C::KS + i;
-                const StreamProb &p = a.p[find_prob_by_step(a, t)];
-                const int64_t o = t - p.step0;
-                const int64_t g = o / p.steps;
-                const int s = (int)(o % p.steps);
+                const StreamProb &p = a.p[pi];
                 const int nblk = s == p.steps - 1 ? p.last_blocks : 8;
-                uint8_t *dst = base + i * L::STEP_BYTES;
-                if (weights) {
-                    const uint8_t *src =
-                        p.W + (g * p.group_vecs + (int64_t)s * (8 * C::VPB + 1)) * kVecBytes;
-                    bulk_g2s(dst, src, (nblk * C::VPB + 1) * kVecBytes, &full[sl]);
-                }
-                if (xs) {
-                    const int xe = min(C::SE, p.K - s * C::SE);
-                    bulk_g2s(dst + L::STEP_WBYTES, p.x + (int64_t)s * C::SE, xe * 4, &full[sl]);
+                const int xe = min(C::SE, p.K - (int)s * C::SE);
+                m[i].g = p.group0 + g;
+                m[i].gs = p.step0 + g * p.steps;
+                m[i].ge = m[i].gs + p.steps;
+                m[i].x = p.x + s * C::SE;
+                m[i].pi = pi;
+                m[i].nblk = nblk;
+                m[i].xe = xe;
+                m[i].step = (int)s;
+                bytes += (nblk * C::VPB + 1) * kVecBytes + xe * 4;
+                if (++s == p.steps) {  // advance the cursor
+                    s = 0;
+                    if (++g == p.groups) {
+                        g = 0;
+                        ++pi;
+                    }
                 }
             }
+            mbar_arrive_expect_tx(&full[sl], bytes);  // releases the metadata too
+            for (int i = 0; i < ns; ++i) {
+                const StreamProb &p = a.p[m[i].pi];
+                const int64_t lg = m[i].g - p.group0;
+                const uint8_t *src =
+                    p.W + (lg * p.group_vecs + (int64_t)m[i].step * SV) * kVecBytes;
+                bulk_g2s(base + i * L::STEP_BYTES, src, (m[i].nblk * C::VPB + 1) * kVecBytes,
+                         &full[sl]);
+            }
+        };
+        auto issue_x = [&](int64_t j) {
+            const int sl = (int)(j % C::S);
+            const int ns = (int)i64min(C::KS, nsteps - j * C::KS);
+            uint8_t *base = ring + sl * L::SLOT_BYTES;
+            const StepMeta *m = meta + sl * C::KS;
+            for (int i = 0; i < ns; ++i)
+                bulk_g2s(base + i * L::STEP_BYTES + L::STEP_WBYTES, m[i].x, m[i].xe * 4, &full[sl]);
         };
         const int64_t nfill = i64min(C::S, nslots);
-        for (int64_t j = 0; j < nfill; ++j) issue(j, true, false);
+        for (int64_t j = 0; j < nfill; ++j) issue_weights(j);
         pdl_wait();  // x may be written by the previous kernel on the stream
-        for (int64_t j = 0; j < nfill; ++j) issue(j, false, true);
+        for (int64_t j = 0; j < nfill; ++j) issue_x(j);
         for (int64_t j = nfill; j < nslots; ++j) {
             const int sl = (int)(j % C::S);
             if (!mbar_wait(&empty[sl], (uint32_t)((j / C::S - 1) & 1), kWaitLimitNs)) {
@@ -322,60 +351,62 @@ __global__ void __launch_bounds__(kStreamThreads, 1) qmm_stream_kernel(const __g
                     mbar_wait(&full[k % C::S], (uint32_t)((k / C::S) & 1), kWaitLimitNs);
                 return;
             }
-            issue(j, true, true);
+            issue_weights(j);
+            issue_x(j);
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    const int si = warp / L::WPS;            // step of the slot this warp works on
+    const int si = warp / L::WPS;             // step of the slot this warp works on
     const int b0 = (warp % L::WPS) * L::BPW;  // its first block in that step
-    const int64_t gfirst = [&] {
+    int64_t gfirst;
+    {
         const StreamProb &p = a.p[find_prob_by_step(a, beg)];
-        return p.group0 + (beg - p.step0) / p.steps;
-    }();
+        gfirst = p.group0 + (beg - p.step0) / p.steps;
+    }
     float acc = 0.f;
-    int64_t cur = -1;  // global group being accumulated
+    int64_t cur = -1, cur_gs = 0, cur_ge = 0;
+    int cur_pi = 0;
 
-    // hand this warp's sum for group g to the CTA; the last contributor
-    // completes the group
-    auto deposit = [&](int64_t g, float v) {
-        const int r = (int)((g - gfirst) % L::R);
-        red[(r * kStreamWarps + warp) * 32 + lane] = v;
+    // hand this warp's sum for its current group to the CTA; the last
+    // contributor completes the group
+    auto deposit = [&]() {
+        const int r = (int)((cur - gfirst) % L::R);
+        red[(r * kStreamWarps + warp) * 32 + lane] = acc;
         __threadfence_block();
         __syncwarp();
         unsigned old = 0;
         if (lane == 0) old = atomicAdd(&gcnt[r], 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
-        // CTA-local steps of g and the warps that touch them
-        const StreamProb &p = a.p[find_prob_by_group(a, g)];
-        const int64_t gs = p.step0 + (g - p.group0) * p.steps, ge = gs + p.steps;
-        const int64_t ls = i64max(gs, beg), le = i64min(ge, end);
+        // warps that touch the group's CTA-local steps
+        const int64_t ls = i64max(cur_gs, beg), le = i64min(cur_ge, end);
         const unsigned expect = (unsigned)(i64min(le - ls, C::KS) * L::WPS);
         if (old + 1 != expect) return;
         __threadfence_block();
-        float s = 0.f;
+        float v = 0.f;
 #pragma unroll
         for (int w = 0; w < kStreamWarps; ++w) {
-            s += red[(r * kStreamWarps + w) * 32 + lane];
+            v += red[(r * kStreamWarps + w) * 32 + lane];
             red[(r * kStreamWarps + w) * 32 + lane] = 0.f;
         }
         __syncwarp();
         if (lane == 0) gcnt[r] = 0;
-        const int64_t n = (g - p.group0) * kRowsPerGroup + lane;
-        if (gs >= beg && ge <= end) {  // the whole group is in this CTA
-            if (n < p.N) p.y[n] = s;
+        const StreamProb &p = a.p[cur_pi];
+        const int64_t n = (cur - p.group0) * kRowsPerGroup + lane;
+        if (cur_gs >= beg && cur_ge <= end) {  // the whole group is in this CTA
+            if (n < p.N) p.y[n] = v;
             return;
         }
         // group split between CTAs (balanced ranges): publish, the last CTA adds up
-        const int side = gs < beg ? 0 : 1;
-        a.part[(cta * 2 + side) * 32 + lane] = s;
+        const int side = cur_gs < beg ? 0 : 1;
+        a.part[(cta * 2 + side) * 32 + lane] = v;
         __threadfence();
         __syncwarp();
         unsigned arrived = 0;
-        if (lane == 0) arrived = atomicAdd(&a.cnt[g], 1u);
+        if (lane == 0) arrived = atomicAdd(&a.cnt[cur], 1u);
         arrived = __shfl_sync(0xffffffffu, arrived, 0);
-        const int64_t i0 = cta_of_step(a, gs), i1 = cta_of_step(a, ge - 1);
+        const int64_t i0 = cta_of_step(a, cur_gs), i1 = cta_of_step(a, cur_ge - 1);
         if (arrived + 1 != (unsigned)(i1 - i0 + 1)) return;
         __threadfence();
         float tot = 0.f;
@@ -384,7 +415,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) qmm_stream_kernel(const __g
             tot += __ldcg(&a.part[(i * 2 + sd) * 32 + lane]);
         }
         if (n < p.N) p.y[n] = tot;
-        if (lane == 0) a.cnt[g] = 0;  // ready for the next call
+        if (lane == 0) a.cnt[cur] = 0;  // ready for the next call
     };
 
     for (int64_t j = 0; j < nslots; ++j) {
@@ -393,27 +424,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1) qmm_stream_kernel(const __g
             if (lane == 0) atomicOr(a.err, kErrFullTimeout);
             return;
         }
-        const int64_t l = j * C::KS + si;
-        if (l < nsteps) {
-            const int64_t t = beg + l;
-            const StreamProb &p = a.p[find_prob_by_step(a, t)];
-            const int64_t o = t - p.step0;
-            const int64_t g = p.group0 + o / p.steps;
-            const int s = (int)(o % p.steps);
-            const int nblk = s == p.steps - 1 ? p.last_blocks : 8;
-            if (g != cur) {
-                if (cur >= 0) deposit(cur, acc);
-                cur = g;
+        if (j * C::KS + si < nsteps) {
+            const StepMeta &m = meta[sl * C::KS + si];
+            if (m.g != cur) {
+                if (cur >= 0) deposit();
+                cur = m.g;
+                cur_gs = m.gs;
+                cur_ge = m.ge;
+                cur_pi = m.pi;
                 acc = 0.f;
             }
             const uint8_t *ws = ring + sl * L::SLOT_BYTES + si * L::STEP_BYTES;
             const float *xs = reinterpret_cast<const float *>(ws + L::STEP_WBYTES);
-            acc += consume_step<FMT>(ws, xs, nblk, b0, lane, a.mg);
+            acc += consume_step<FMT>(ws, xs, m.nblk, b0, lane, a.mg);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sl]);
     }
-    if (cur >= 0) deposit(cur, acc);
+    if (cur >= 0) deposit();
 }
 
 }  // namespace lean
