@@ -11,7 +11,7 @@
 namespace lean {
 
 constexpr int kMaxBatch = LEAN_MAX_BATCH;  // problems per batched launch
-constexpr int kMaxStreamCtas = 256;        // CTAs of one streaming launch, at most
+constexpr int kMaxStreamCtas = 512;        // CTAs of one streaming launch, at most
 
 struct HostProb {
     const uint8_t *W;

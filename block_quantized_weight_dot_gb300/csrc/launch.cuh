@@ -234,7 +234,7 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
     a.total_groups = groups;
     a.mg = make_magic();
     a.err = err;
-    const int64_t sms = std::min<int64_t>(sm_count(), kMaxStreamCtas);
+    const int64_t sms = std::min<int64_t>((int64_t)sm_count() * C::CPS, kMaxStreamCtas);
     if (ws != nullptr) {
         const WorkspaceLayout wl = workspace_layout(groups);
         if (ws_bytes < wl.total) return LEAN_ERR_SHAPE;

@@ -70,11 +70,12 @@ struct StreamArgs {
 
 template <int FMT> struct StreamCfg;
 // VPB: quant vectors per block; SE: x elements per step; KS: steps per slot;
-// S: slots in the ring.  A slot is about 20-60 KB; the ring about 150-190 KB.
-template <> struct StreamCfg<Q4_0> { static constexpr int VPB = 1, SE = 256, KS = 4, S = 6; };
-template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, SE = 256, KS = 4, S = 4; };
-template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, SE = 512, KS = 2, S = 4; };
-template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, SE = 2048, KS = 1, S = 3; };
+// S: slots in the ring; CPS: CTAs per SM.  A slot is about 20-60 KB; an SM
+// holds about 110-190 KB of ring in all.
+template <> struct StreamCfg<Q4_0> { static constexpr int VPB = 1, SE = 256, KS = 4, S = 3, CPS = 2; };
+template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, SE = 256, KS = 4, S = 2, CPS = 2; };
+template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, SE = 512, KS = 2, S = 2, CPS = 2; };
+template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, SE = 2048, KS = 1, S = 3, CPS = 1; };
 
 template <int FMT>
 struct StreamLayout {
@@ -247,7 +248,7 @@ struct StepMeta {
 static_assert(sizeof(StepMeta) == 48, "StepMeta layout");
 
 template <int FMT, int NP>
-__global__ void __launch_bounds__(kStreamThreads, 1)
+__global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     qmm_stream_kernel(const __grid_constant__ StreamArgs<NP> a) {
     using C = StreamCfg<FMT>;
     using L = StreamLayout<FMT>;
