@@ -70,9 +70,10 @@ struct StreamArgs {
 
 template <int FMT> struct StreamCfg;
 // VPB: quant vectors per block; SE: x elements per step; KS: steps per slot;
-// S: slots in the ring; CPS: CTAs per SM.  A slot is about 20-60 KB; an SM
-// holds about 110-190 KB of ring in all.
-template <> struct StreamCfg<Q4_0> { static constexpr int VPB = 1, SE = 256, KS = 4, S = 3, CPS = 2; };
+// S: slots in the ring; CPS: CTAs per SM.  Each consumer warp handles BPW
+// blocks of one step per slot (128 or 256 weights per lane); an SM holds
+// about 90-190 KB of ring in all.
+template <> struct StreamCfg<Q4_0> { static constexpr int VPB = 1, SE = 256, KS = 8, S = 2, CPS = 2; };
 template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, SE = 256, KS = 4, S = 2, CPS = 2; };
 template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, SE = 512, KS = 2, S = 2, CPS = 2; };
 template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, SE = 2048, KS = 1, S = 3, CPS = 1; };
@@ -86,14 +87,14 @@ struct StreamLayout {
     static constexpr int SLOT_BYTES = C::KS * STEP_BYTES;
     static constexpr int WPS = kStreamWarps / C::KS;  // warps per step
     static constexpr int BPW = 8 / WPS;               // blocks per warp
-    static constexpr int R = (C::S + 1) * C::KS + 3;  // ring of groups being reduced
-    // shared memory: [full S][empty S][meta S*KS][cnt R][red R*W*32][pad][ring S*SLOT]
+    // shared memory: [full S][empty S][meta S*KS][stage 2*W*32][carry 2*32][abort][ring S*SLOT]
     static constexpr int OFF_FULL = 0;
     static constexpr int OFF_EMPTY = 8 * C::S;
     static constexpr int OFF_META = 16 * C::S;
-    static constexpr int OFF_CNT = OFF_META + 48 * C::S * C::KS;
-    static constexpr int OFF_RED = OFF_CNT + 4 * R;
-    static constexpr int OFF_RING = ((OFF_RED + 4 * R * kStreamWarps * 32) + 127) / 128 * 128;
+    static constexpr int OFF_STAGE = OFF_META + 48 * C::S * C::KS;
+    static constexpr int OFF_CARRY = OFF_STAGE + 4 * 2 * kStreamWarps * 32;
+    static constexpr int OFF_ABORT = OFF_CARRY + 4 * 2 * 32;
+    static constexpr int OFF_RING = (OFF_ABORT + 16 + 127) / 128 * 128;
     static constexpr int SMEM = OFF_RING + C::S * SLOT_BYTES;
 };
 
@@ -140,99 +141,121 @@ __device__ __forceinline__ int64_t cta_of_step(const StreamArgs<NP> &a, int64_t 
 }
 
 // ---- per-format consumer work on one step held in shared memory -------------
-// Returns this warp's share of sum_k w x for its lane's row, blocks [b0, b0+BPW).
+// One block: this lane's row, block b of the step at ws, x of the block at xb.
 template <int FMT>
-__device__ __forceinline__ float consume_step(const uint8_t *ws, const float *xs, int nblk, int b0,
+__device__ __forceinline__ float block_dot(const uint8_t *ws, const float *xb, int b, float d,
+                                           int lane, const Magic &mg) {
+    using C = StreamCfg<FMT>;
+    if (FMT == Q4_0) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(ws + b * kVecBytes + lane * 16);
+        f32x2 s = 0ull;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            f32x2 p[4];
+            q4_word(word_of(v, t), mg, p);
+            const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t);
+            const ulonglong2 xc = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t + 4);
+            s = fma2(p[0], xa.x, s);
+            s = fma2(p[1], xa.y, s);
+            s = fma2(p[2], xc.x, s);
+            s = fma2(p[3], xc.y, s);
+        }
+        const float2 r = unpack2(s);
+        return d * (r.x + r.y);
+    } else if (FMT == Q8_0 || FMT == I8_B64) {
+        f32x2 s = 0ull;
+#pragma unroll
+        for (int j = 0; j < C::VPB; ++j) {
+            const uint4 v =
+                *reinterpret_cast<const uint4 *>(ws + (b * C::VPB + j) * kVecBytes + lane * 16);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                f32x2 p[2];
+                i8_word(word_of(v, t), mg, p);
+                const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xb + j * 16 + 4 * t);
+                s = fma2(p[0], xa.x, s);
+                s = fma2(p[1], xa.y, s);
+            }
+        }
+        const float2 r = unpack2(s);
+        return d * (r.x + r.y);
+    } else {  // Q6_K super-block: 16 sub-blocks with int8 sub-scales
+        const uint8_t *sb = ws + b * C::VPB * kVecBytes + lane * 16;
+        const uint4 scv = *reinterpret_cast<const uint4 *>(sb + 12 * kVecBytes);
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // 4 sub-blocks per 3 vectors
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(sb + (3 * q + 0) * kVecBytes);
+            const uint4 v1 = *reinterpret_cast<const uint4 *>(sb + (3 * q + 1) * kVecBytes);
+            const uint4 v2 = *reinterpret_cast<const uint4 *>(sb + (3 * q + 2) * kVecBytes);
+            const uint32_t w[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y,
+                                    v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int sub = 4 * q + u;
+                f32x2 p[8];
+                q6_group(w[3 * u], w[3 * u + 1], w[3 * u + 2], mg, p);
+                f32x2 s = 0ull;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const ulonglong2 xa =
+                        *reinterpret_cast<const ulonglong2 *>(xb + sub * 16 + 4 * j);
+                    s = fma2(p[2 * j], xa.x, s);
+                    s = fma2(p[2 * j + 1], xa.y, s);
+                }
+                const float sc = i8_byte(word_of(scv, sub >> 2), sub & 3, mg);
+                const float2 r = unpack2(s);
+                acc = fmaf(d * sc, r.x + r.y, acc);
+            }
+        }
+        return acc;
+    }
+}
+
+// This warp's share of sum_k w x for its lane's row: blocks [B0, B0+BPW) of a
+// step with nblk blocks.  B0 is a compile-time constant so that every shared
+// address below is a constant offset; full steps take the unchecked path.
+template <int FMT, int B0>
+__device__ __forceinline__ float consume_step(const uint8_t *ws, const float *xs, int nblk,
                                               int lane, const Magic &mg) {
     using C = StreamCfg<FMT>;
     constexpr int BPW = StreamLayout<FMT>::BPW;
-    const uint4 sv = *reinterpret_cast<const uint4 *>(ws + nblk * C::VPB * kVecBytes + lane * 16);
     float acc = 0.f;
-    if (FMT == Q4_0) {
+    if (nblk == 8) {
+        const uint4 sv =
+            *reinterpret_cast<const uint4 *>(ws + 8 * C::VPB * kVecBytes + lane * 16);
 #pragma unroll
-        for (int i = 0; i < BPW; ++i) {
-            const int b = b0 + i;
-            if (b < nblk) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(ws + b * kVecBytes + lane * 16);
-                const float *xb = xs + b * 32;
-                f32x2 s = 0ull;
+        for (int i = 0; i < BPW; ++i)
+            acc += block_dot<FMT>(ws, xs + (B0 + i) * (C::SE / 8), B0 + i, scale_of(sv, B0 + i),
+                                  lane, mg);
+    } else {
+        const uint4 sv =
+            *reinterpret_cast<const uint4 *>(ws + nblk * C::VPB * kVecBytes + lane * 16);
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    f32x2 p[4];
-                    q4_word(word_of(v, t), mg, p);
-                    const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t);
-                    const ulonglong2 xc = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t + 4);
-                    s = fma2(p[0], xa.x, s);
-                    s = fma2(p[1], xa.y, s);
-                    s = fma2(p[2], xc.x, s);
-                    s = fma2(p[3], xc.y, s);
-                }
-                const float2 r = unpack2(s);
-                acc = fmaf(scale_of(sv, b), r.x + r.y, acc);
-            }
-        }
-    } else if (FMT == Q8_0 || FMT == I8_B64) {
-#pragma unroll
-        for (int i = 0; i < BPW; ++i) {
-            const int b = b0 + i;
-            if (b < nblk) {
-                f32x2 s = 0ull;
-#pragma unroll
-                for (int j = 0; j < C::VPB; ++j) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(
-                        ws + (b * C::VPB + j) * kVecBytes + lane * 16);
-                    const float *xb = xs + (b * C::VPB + j) * 16;
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        f32x2 p[2];
-                        i8_word(word_of(v, t), mg, p);
-                        const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xb + 4 * t);
-                        s = fma2(p[0], xa.x, s);
-                        s = fma2(p[1], xa.y, s);
-                    }
-                }
-                const float2 r = unpack2(s);
-                acc = fmaf(scale_of(sv, b), r.x + r.y, acc);
-            }
-        }
-    } else {  // Q6_K: one super-block per warp, 16 sub-blocks with int8 sub-scales
-#pragma unroll
-        for (int i = 0; i < BPW; ++i) {
-            const int b = b0 + i;
-            if (b < nblk) {
-                const uint8_t *sb = ws + b * C::VPB * kVecBytes + lane * 16;
-                const float d = scale_of(sv, b);
-                const uint4 scv = *reinterpret_cast<const uint4 *>(sb + 12 * kVecBytes);
-                const float *xb = xs + b * 256;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {  // 4 sub-blocks per 3 vectors
-                    const uint4 v0 = *reinterpret_cast<const uint4 *>(sb + (3 * q + 0) * kVecBytes);
-                    const uint4 v1 = *reinterpret_cast<const uint4 *>(sb + (3 * q + 1) * kVecBytes);
-                    const uint4 v2 = *reinterpret_cast<const uint4 *>(sb + (3 * q + 2) * kVecBytes);
-                    const uint32_t w[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y,
-                                            v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int sub = 4 * q + u;
-                        f32x2 p[8];
-                        q6_group(w[3 * u], w[3 * u + 1], w[3 * u + 2], mg, p);
-                        f32x2 s = 0ull;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const ulonglong2 xa =
-                                *reinterpret_cast<const ulonglong2 *>(xb + sub * 16 + 4 * j);
-                            s = fma2(p[2 * j], xa.x, s);
-                            s = fma2(p[2 * j + 1], xa.y, s);
-                        }
-                        const float sc = i8_byte(word_of(scv, sub >> 2), sub & 3, mg);
-                        const float2 r = unpack2(s);
-                        acc = fmaf(d * sc, r.x + r.y, acc);
-                    }
-                }
-            }
-        }
+        for (int i = 0; i < BPW; ++i)
+            if (B0 + i < nblk)
+                acc += block_dot<FMT>(ws, xs + (B0 + i) * (C::SE / 8), B0 + i,
+                                      scale_of(sv, B0 + i), lane, mg);
     }
     return acc;
+}
+
+// dispatch on the warp's (runtime) first block
+template <int FMT>
+__device__ __forceinline__ float consume(const uint8_t *ws, const float *xs, int nblk, int b0,
+                                         int lane, const Magic &mg) {
+    constexpr int BPW = StreamLayout<FMT>::BPW;
+    switch (b0 / BPW) {
+    case 0: return consume_step<FMT, 0>(ws, xs, nblk, lane, mg);
+    case 1: if (BPW * 1 < 8) return consume_step<FMT, (BPW * 1) % 8>(ws, xs, nblk, lane, mg); break;
+    case 2: if (BPW * 2 < 8) return consume_step<FMT, (BPW * 2) % 8>(ws, xs, nblk, lane, mg); break;
+    case 3: if (BPW * 3 < 8) return consume_step<FMT, (BPW * 3) % 8>(ws, xs, nblk, lane, mg); break;
+    case 4: if (BPW * 4 < 8) return consume_step<FMT, (BPW * 4) % 8>(ws, xs, nblk, lane, mg); break;
+    case 5: if (BPW * 5 < 8) return consume_step<FMT, (BPW * 5) % 8>(ws, xs, nblk, lane, mg); break;
+    case 6: if (BPW * 6 < 8) return consume_step<FMT, (BPW * 6) % 8>(ws, xs, nblk, lane, mg); break;
+    case 7: if (BPW * 7 < 8) return consume_step<FMT, (BPW * 7) % 8>(ws, xs, nblk, lane, mg); break;
+    }
+    return 0.f;
 }
 
 // What the producer learned about one step of a slot, for the consumers.
@@ -256,9 +279,10 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     extern __shared__ __align__(128) uint8_t sbuf[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sbuf + L::OFF_FULL);
     uint64_t *empty = reinterpret_cast<uint64_t *>(sbuf + L::OFF_EMPTY);
-    unsigned *gcnt = reinterpret_cast<unsigned *>(sbuf + L::OFF_CNT);
-    float *red = reinterpret_cast<float *>(sbuf + L::OFF_RED);
     StepMeta *meta = reinterpret_cast<StepMeta *>(sbuf + L::OFF_META);
+    float *stage = reinterpret_cast<float *>(sbuf + L::OFF_STAGE);   // [2][W][32]
+    float *carry = reinterpret_cast<float *>(sbuf + L::OFF_CARRY);   // [2][32]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sbuf + L::OFF_ABORT);
     uint8_t *ring = sbuf + L::OFF_RING;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -276,9 +300,8 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             mbar_init(&empty[s], kStreamWarps);
         }
         fence_mbar_init();
+        *abort_flag = 0;
     }
-    for (int i = threadIdx.x; i < L::R; i += blockDim.x) gcnt[i] = 0;
-    for (int i = threadIdx.x; i < L::R * kStreamWarps * 32; i += blockDim.x) red[i] = 0.f;
     __syncthreads();
     if (nsteps <= 0) return;
 
@@ -293,7 +316,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             g = o / a.p[pi].steps;
             s = o % a.p[pi].steps;
         }
-        // fill the metadata of slot j and copy its weights; returns the bytes armed
+        // fill the metadata of slot j, arm its barrier and copy its weights
         auto issue_weights = [&](int64_t j) {
             const int sl = (int)(j % C::S);
             const int ns = (int)i64min(C::KS, nsteps - j * C::KS);
@@ -345,7 +368,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
         for (int64_t j = 0; j < nfill; ++j) issue_x(j);
         for (int64_t j = nfill; j < nslots; ++j) {
             const int sl = (int)(j % C::S);
-            if (!mbar_wait(&empty[sl], (uint32_t)((j / C::S - 1) & 1), kWaitLimitNs)) {
+            if (*abort_flag || !mbar_wait(&empty[sl], (uint32_t)((j / C::S - 1) & 1), kWaitLimitNs)) {
                 atomicOr(a.err, kErrEmptyTimeout);
                 // let the copies already issued land before the CTA can exit
                 for (int64_t k = i64max(0, j - C::S); k < j; ++k)
@@ -359,55 +382,32 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     }
 
     // ---------------------------------------------------------------- consumers
+    // Each warp computes its blocks of one step per slot and stages its sum;
+    // after a barrier of the consumer warps, warp r adds up run r of the slot
+    // (consecutive steps of one row group) in step order, carrying a group
+    // that continues into the next slot.  A group complete in this CTA is
+    // stored; one shared with other CTAs (workspace mode) is published and
+    // finished by the last CTA.  Every sum is taken in a fixed order.
     const int si = warp / L::WPS;             // step of the slot this warp works on
     const int b0 = (warp % L::WPS) * L::BPW;  // its first block in that step
-    int64_t gfirst;
-    {
-        const StreamProb &p = a.p[find_prob_by_step(a, beg)];
-        gfirst = p.group0 + (beg - p.step0) / p.steps;
-    }
-    float acc = 0.f;
-    int64_t cur = -1, cur_gs = 0, cur_ge = 0;
-    int cur_pi = 0;
 
-    // hand this warp's sum for its current group to the CTA; the last
-    // contributor completes the group
-    auto deposit = [&]() {
-        const int r = (int)((cur - gfirst) % L::R);
-        red[(r * kStreamWarps + warp) * 32 + lane] = acc;
-        __threadfence_block();
-        __syncwarp();
-        unsigned old = 0;
-        if (lane == 0) old = atomicAdd(&gcnt[r], 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        // warps that touch the group's CTA-local steps
-        const int64_t ls = i64max(cur_gs, beg), le = i64min(cur_ge, end);
-        const unsigned expect = (unsigned)(i64min(le - ls, C::KS) * L::WPS);
-        if (old + 1 != expect) return;
-        __threadfence_block();
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kStreamWarps; ++w) {
-            v += red[(r * kStreamWarps + w) * 32 + lane];
-            red[(r * kStreamWarps + w) * 32 + lane] = 0.f;
-        }
-        __syncwarp();
-        if (lane == 0) gcnt[r] = 0;
-        const StreamProb &p = a.p[cur_pi];
-        const int64_t n = (cur - p.group0) * kRowsPerGroup + lane;
-        if (cur_gs >= beg && cur_ge <= end) {  // the whole group is in this CTA
+    // finish the CTA's part of group g (global steps [gs, ge), problem pi) with value v
+    auto finish_group = [&](int64_t g, int64_t gs, int64_t ge, int pi, float v) {
+        const StreamProb &p = a.p[pi];
+        const int64_t n = (g - p.group0) * kRowsPerGroup + lane;
+        if (gs >= beg && ge <= end) {  // the whole group is in this CTA
             if (n < p.N) p.y[n] = v;
             return;
         }
-        // group split between CTAs (balanced ranges): publish, the last CTA adds up
-        const int side = cur_gs < beg ? 0 : 1;
+        // group split between CTAs: publish, the last CTA to arrive adds up
+        const int side = gs < beg ? 0 : 1;
         a.part[(cta * 2 + side) * 32 + lane] = v;
         __threadfence();
         __syncwarp();
         unsigned arrived = 0;
-        if (lane == 0) arrived = atomicAdd(&a.cnt[cur], 1u);
+        if (lane == 0) arrived = atomicAdd(&a.cnt[g], 1u);
         arrived = __shfl_sync(0xffffffffu, arrived, 0);
-        const int64_t i0 = cta_of_step(a, cur_gs), i1 = cta_of_step(a, cur_ge - 1);
+        const int64_t i0 = cta_of_step(a, gs), i1 = cta_of_step(a, ge - 1);
         if (arrived + 1 != (unsigned)(i1 - i0 + 1)) return;
         __threadfence();
         float tot = 0.f;
@@ -416,33 +416,57 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             tot += __ldcg(&a.part[(i * 2 + sd) * 32 + lane]);
         }
         if (n < p.N) p.y[n] = tot;
-        if (lane == 0) a.cnt[cur] = 0;  // ready for the next call
+        if (lane == 0) a.cnt[g] = 0;  // ready for the next call
     };
 
     for (int64_t j = 0; j < nslots; ++j) {
         const int sl = (int)(j % C::S);
-        if (!mbar_wait(&full[sl], (uint32_t)((j / C::S) & 1), kWaitLimitNs)) {
-            if (lane == 0) atomicOr(a.err, kErrFullTimeout);
-            return;
+        const int ns = (int)i64min(C::KS, nsteps - j * C::KS);
+        const bool ok = mbar_wait(&full[sl], (uint32_t)((j / C::S) & 1), kWaitLimitNs);
+        if (!ok && lane == 0) {
+            atomicOr(a.err, kErrFullTimeout);
+            *abort_flag = 1;
         }
-        if (j * C::KS + si < nsteps) {
+        float v = 0.f;
+        if (ok && si < ns) {
             const StepMeta &m = meta[sl * C::KS + si];
-            if (m.g != cur) {
-                if (cur >= 0) deposit();
-                cur = m.g;
-                cur_gs = m.gs;
-                cur_ge = m.ge;
-                cur_pi = m.pi;
-                acc = 0.f;
-            }
             const uint8_t *ws = ring + sl * L::SLOT_BYTES + si * L::STEP_BYTES;
             const float *xs = reinterpret_cast<const float *>(ws + L::STEP_WBYTES);
-            acc += consume_step<FMT>(ws, xs, m.nblk, b0, lane, a.mg);
+            v = consume<FMT>(ws, xs, m.nblk, b0, lane, a.mg);
+        }
+        float *stg = stage + (j & 1) * kStreamWarps * 32;
+        stg[warp * 32 + lane] = v;
+        named_barrier_sync(1, 32 * kStreamWarps);  // every consumer warp staged its sum
+        // all consumer warps read the flag after the same barrier: they stop together
+        if (*abort_flag) return;
+        {
+            // run r of the slot: the r-th maximal run of steps with one group
+            const StepMeta *m = meta + sl * C::KS;
+            int r = 0, i0 = 0;
+            for (int i = 1; i <= ns && r <= warp; ++i) {
+                if (i == ns || m[i].g != m[i0].g) {
+                    if (r == warp) {
+                        const StepMeta &mm = m[i0];
+                        float sum = 0.f;
+                        const int64_t t0 = beg + j * C::KS + i0;
+                        if (t0 != mm.gs && t0 != beg)  // continues a run of the previous slot
+                            sum = carry[((j + 1) & 1) * 32 + lane];
+                        for (int k = i0 * L::WPS; k < i * L::WPS; ++k) sum += stg[k * 32 + lane];
+                        const int64_t t1 = beg + j * C::KS + i;  // one past the run
+                        if (t1 == i64min(mm.ge, end)) {
+                            finish_group(mm.g, mm.gs, mm.ge, mm.pi, sum);
+                        } else {  // the group goes on in the next slot
+                            carry[(j & 1) * 32 + lane] = sum;
+                        }
+                    }
+                    ++r;
+                    i0 = i;
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sl]);
     }
-    if (cur >= 0) deposit();
 }
 
 }  // namespace lean
