@@ -14,6 +14,7 @@
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "ptx.cuh"
 
@@ -21,11 +22,61 @@ namespace lean {
 
 struct Magic {
     uint32_t m0, m4, m6, m8, m12, m14, m16;  // bit p of the mantissa worth 1.0
+    uint32_t pad;
+    // (bias + offset) pairs subtracted after the LOP3, as f32x2 bit patterns
+    unsigned long long q4[4];  // Q4_0 element pairs (0,1) (2,3) (4,5) (6,7) of a word
+    unsigned long long i8;     // int8 byte pairs (0,1) / (2,3)
+    unsigned long long q6[8];  // Q6_K element pairs of a sub-block
 };
+inline unsigned long long f2_bits(float lo, float hi) {
+    uint32_t a, b;
+    memcpy(&a, &lo, 4);
+    memcpy(&b, &hi, 4);
+    return ((unsigned long long)b << 32) | a;
+}
 inline Magic make_magic() {
     // exponent field 150 - p: the float 2^(23-p) has mantissa bit p worth 1
-    return Magic{0x4B000000u, 0x49000000u, 0x48000000u, 0x47000000u,
-                 0x45000000u, 0x44000000u, 0x43000000u};
+    Magic m;
+    m.m0 = 0x4B000000u; m.m4 = 0x49000000u; m.m6 = 0x48000000u; m.m8 = 0x47000000u;
+    m.m12 = 0x45000000u; m.m14 = 0x44000000u; m.m16 = 0x43000000u; m.pad = 0;
+    // Q4_0: bias 2^(23-p) plus the offset 8
+    m.q4[0] = f2_bits(-8388616.0f, -524296.0f);  // p = 0, 4
+    m.q4[1] = f2_bits(-32776.0f, -2056.0f);      // p = 8, 12
+    m.q4[2] = f2_bits(-136.0f, -32776.0f);       // p = 16, 8
+    m.q4[3] = f2_bits(-2056.0f, -136.0f);        // p = 12, 16
+    m.i8 = f2_bits(-8388736.0f, -32896.0f);      // bias 2^23 / 2^15 plus 128
+    const float c0 = -8388640.0f, c6 = -131104.0f, c12 = -2080.0f, c14 = -544.0f;  // + 32
+    m.q6[0] = f2_bits(c0, c6);
+    m.q6[1] = f2_bits(c12, c6);
+    m.q6[2] = f2_bits(c12, c0);
+    m.q6[3] = f2_bits(c6, c12);
+    m.q6[4] = f2_bits(c6, c12);
+    m.q6[5] = f2_bits(c0, c6);
+    m.q6[6] = f2_bits(c12, c6);
+    m.q6[7] = f2_bits(c12, c14);
+    return m;
+}
+
+// Copy the constants into registers once per thread: the opaque moves keep
+// the compiler from re-materialising them inside the streaming loops.
+__device__ __forceinline__ uint32_t pin32(uint32_t v) {
+    asm volatile("mov.b32 %0, %0;" : "+r"(v));
+    return v;
+}
+__device__ __forceinline__ unsigned long long pin64(unsigned long long v) {
+    asm volatile("mov.b64 %0, %0;" : "+l"(v));
+    return v;
+}
+__device__ __forceinline__ Magic pin(const Magic &g) {
+    Magic m;
+    m.m0 = pin32(g.m0); m.m4 = pin32(g.m4); m.m6 = pin32(g.m6); m.m8 = pin32(g.m8);
+    m.m12 = pin32(g.m12); m.m14 = pin32(g.m14); m.m16 = pin32(g.m16); m.pad = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m.q4[i] = pin64(g.q4[i]);
+    m.i8 = pin64(g.i8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m.q6[i] = pin64(g.q6[i]);
+    return m;
 }
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
@@ -35,22 +86,23 @@ __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ void q4_word(uint32_t w, const Magic &mg, f32x2 p[4]) {
     const uint32_t h = w >> 12;  // nibbles 5, 6, 7 -> bits 8, 12, 16
     p[0] = add2(pack2(as_f(and_or(w, 0x0000000Fu, mg.m0)), as_f(and_or(w, 0x000000F0u, mg.m4))),
-                pack2(-8388616.0f, -524296.0f));  // 2^23 + 8, 2^19 + 8
+                mg.q4[0]);
     p[1] = add2(pack2(as_f(and_or(w, 0x00000F00u, mg.m8)), as_f(and_or(w, 0x0000F000u, mg.m12))),
-                pack2(-32776.0f, -2056.0f));      // 2^15 + 8, 2^11 + 8
+                mg.q4[1]);
     p[2] = add2(pack2(as_f(and_or(w, 0x000F0000u, mg.m16)), as_f(and_or(h, 0x00000F00u, mg.m8))),
-                pack2(-136.0f, -32776.0f));       // 2^7 + 8
+                mg.q4[2]);
     p[3] = add2(pack2(as_f(and_or(h, 0x0000F000u, mg.m12)), as_f(and_or(h, 0x000F0000u, mg.m16))),
-                pack2(-2056.0f, -136.0f));
+                mg.q4[3]);
 }
 
 // ---- int8 stored + 128: one word = 4 elements, byte i = element i ------------
 // p[0] = (q0, q1), p[1] = (q2, q3)
 __device__ __forceinline__ void i8_word(uint32_t w, const Magic &mg, f32x2 p[2]) {
     const uint32_t h = w >> 16;
-    const f32x2 c = pack2(-8388736.0f, -32896.0f);  // 2^23 + 128, 2^15 + 128
-    p[0] = add2(pack2(as_f(and_or(w, 0x000000FFu, mg.m0)), as_f(and_or(w, 0x0000FF00u, mg.m8))), c);
-    p[1] = add2(pack2(as_f(and_or(h, 0x000000FFu, mg.m0)), as_f(and_or(h, 0x0000FF00u, mg.m8))), c);
+    p[0] = add2(pack2(as_f(and_or(w, 0x000000FFu, mg.m0)), as_f(and_or(w, 0x0000FF00u, mg.m8))),
+                mg.i8);
+    p[1] = add2(pack2(as_f(and_or(h, 0x000000FFu, mg.m0)), as_f(and_or(h, 0x0000FF00u, mg.m8))),
+                mg.i8);
 }
 
 // ---- Q6_K sub-block: 3 words = 16 six-bit values --------------------------------
@@ -63,25 +115,21 @@ __device__ __forceinline__ void q6_group(uint32_t w0, uint32_t w1, uint32_t w2, 
     uint32_t e15 = and_or(s0, 0x000C0000u, mg.m14);
     e15 = and_or(w1 >> 14, 0x00030000u, e15);
     e15 = and_or(w2 >> 16, 0x0000C000u, e15);
-    const float c0 = -8388640.0f;  // 2^23 + 32
-    const float c6 = -131104.0f;   // 2^17 + 32
-    const float c12 = -2080.0f;    // 2^11 + 32
-    const float c14 = -544.0f;     // 2^9 + 32
     p[0] = add2(pack2(as_f(and_or(w0, 0x0000003Fu, mg.m0)), as_f(and_or(w0, 0x00000FC0u, mg.m6))),
-                pack2(c0, c6));
+                mg.q6[0]);
     p[1] = add2(pack2(as_f(and_or(w0, 0x0003F000u, mg.m12)), as_f(and_or(s0, 0x00000FC0u, mg.m6))),
-                pack2(c12, c6));
+                mg.q6[1]);
     p[2] = add2(pack2(as_f(and_or(s0, 0x0003F000u, mg.m12)), as_f(and_or(w1, 0x0000003Fu, mg.m0))),
-                pack2(c12, c0));
+                mg.q6[2]);
     p[3] = add2(pack2(as_f(and_or(w1, 0x00000FC0u, mg.m6)), as_f(and_or(w1, 0x0003F000u, mg.m12))),
-                pack2(c6, c12));
+                mg.q6[3]);
     p[4] = add2(pack2(as_f(and_or(s1, 0x00000FC0u, mg.m6)), as_f(and_or(s1, 0x0003F000u, mg.m12))),
-                pack2(c6, c12));
+                mg.q6[4]);
     p[5] = add2(pack2(as_f(and_or(w2, 0x0000003Fu, mg.m0)), as_f(and_or(w2, 0x00000FC0u, mg.m6))),
-                pack2(c0, c6));
+                mg.q6[5]);
     p[6] = add2(pack2(as_f(and_or(w2, 0x0003F000u, mg.m12)), as_f(and_or(s2, 0x00000FC0u, mg.m6))),
-                pack2(c12, c6));
-    p[7] = add2(pack2(as_f(and_or(s2, 0x0003F000u, mg.m12)), as_f(e15)), pack2(c12, c14));
+                mg.q6[6]);
+    p[7] = add2(pack2(as_f(and_or(s2, 0x0003F000u, mg.m12)), as_f(e15)), mg.q6[7]);
 }
 
 // int8 sub-scale stored + 128, byte i of word w

@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
     const uint8_t *grp = a.W + (g * a.group_vecs) * kVecBytes + lane * kVec;
 
     pdl_launch_dependents();
+    const Magic mg = pin(a.mg);
     BlockFrag<FMT> fa, fb;
     if (w0 < w1) load_block<FMT>(fa, a, grp, w0);
     pdl_wait();  // x may come from the previous kernel on the stream
@@ -187,9 +188,9 @@ __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
     for (int m = 0; m < MT; ++m) tot[m] = 0.f;
     for (int64_t c = w0; c < w1; c += 2) {
         if (c + 1 < w1) load_block<FMT>(fb, a, grp, c + 1);
-        block_fma<FMT, MT>(fa, xs + (c - c0) * E, a.xs_stride, a.mg, tot);
+        block_fma<FMT, MT>(fa, xs + (c - c0) * E, a.xs_stride, mg, tot);
         if (c + 2 < w1) load_block<FMT>(fa, a, grp, c + 2);
-        if (c + 1 < w1) block_fma<FMT, MT>(fb, xs + (c + 1 - c0) * E, a.xs_stride, a.mg, tot);
+        if (c + 1 < w1) block_fma<FMT, MT>(fb, xs + (c + 1 - c0) * E, a.xs_stride, mg, tot);
     }
 
     // reduce over the wpr warps of each row group: red[warp][m][lane]

@@ -240,11 +240,29 @@ __device__ __forceinline__ float consume_step(const uint8_t *ws, const float *xs
     return acc;
 }
 
-// dispatch on the warp's (runtime) first block
+// This warp's share with a runtime first block (one code copy for all warps).
+template <int FMT>
+__device__ __forceinline__ float consume_any(const uint8_t *ws, const float *xs, int nblk, int b0,
+                                             int lane, const Magic &mg) {
+    using C = StreamCfg<FMT>;
+    constexpr int BPW = StreamLayout<FMT>::BPW;
+    const uint4 sv = *reinterpret_cast<const uint4 *>(ws + nblk * C::VPB * kVecBytes + lane * 16);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < BPW; ++i) {
+        const int b = b0 + i;
+        if (b < nblk) acc += block_dot<FMT>(ws, xs + b * (C::SE / 8), b, scale_of(sv, b), lane, mg);
+    }
+    return acc;
+}
+
+// dispatch on the warp's (runtime) first block: compile-time offsets when a
+// step is split over at most two warps, a single code copy otherwise
 template <int FMT>
 __device__ __forceinline__ float consume(const uint8_t *ws, const float *xs, int nblk, int b0,
                                          int lane, const Magic &mg) {
     constexpr int BPW = StreamLayout<FMT>::BPW;
+    if (8 / BPW > 2) return consume_any<FMT>(ws, xs, nblk, b0, lane, mg);
     switch (b0 / BPW) {
     case 0: return consume_step<FMT, 0>(ws, xs, nblk, lane, mg);
     case 1: if (BPW * 1 < 8) return consume_step<FMT, (BPW * 1) % 8>(ws, xs, nblk, lane, mg); break;
@@ -390,6 +408,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     // finished by the last CTA.  Every sum is taken in a fixed order.
     const int si = warp / L::WPS;             // step of the slot this warp works on
     const int b0 = (warp % L::WPS) * L::BPW;  // its first block in that step
+    const Magic mg = pin(a.mg);
 
     // finish the CTA's part of group g (global steps [gs, ge), problem pi) with value v
     auto finish_group = [&](int64_t g, int64_t gs, int64_t ge, int pi, float v) {
@@ -432,7 +451,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             const StepMeta &m = meta[sl * C::KS + si];
             const uint8_t *ws = ring + sl * L::SLOT_BYTES + si * L::STEP_BYTES;
             const float *xs = reinterpret_cast<const float *>(ws + L::STEP_WBYTES);
-            v = consume<FMT>(ws, xs, m.nblk, b0, lane, a.mg);
+            v = consume<FMT>(ws, xs, m.nblk, b0, lane, mg);
         }
         float *stg = stage + (j & 1) * kStreamWarps * 32;
         stg[warp * 32 + lane] = v;
