@@ -148,22 +148,22 @@ __device__ __forceinline__ float block_dot(const uint8_t *ws, const float *xb, i
     using C = StreamCfg<FMT>;
     if (FMT == Q4_0) {
         const uint4 v = *reinterpret_cast<const uint4 *>(ws + b * kVecBytes + lane * 16);
-        f32x2 s = 0ull;
+        f32x2 s[4];  // one chain per word: four independent FMA chains
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             f32x2 p[4];
             q4_word(word_of(v, t), mg, p);
             const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t);
             const ulonglong2 xc = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t + 4);
-            s = fma2(p[0], xa.x, s);
-            s = fma2(p[1], xa.y, s);
-            s = fma2(p[2], xc.x, s);
-            s = fma2(p[3], xc.y, s);
+            s[t] = mul2(p[0], xa.x);
+            s[t] = fma2(p[1], xa.y, s[t]);
+            s[t] = fma2(p[2], xc.x, s[t]);
+            s[t] = fma2(p[3], xc.y, s[t]);
         }
-        const float2 r = unpack2(s);
+        const float2 r = unpack2(add2(add2(s[0], s[1]), add2(s[2], s[3])));
         return d * (r.x + r.y);
     } else if (FMT == Q8_0 || FMT == I8_B64) {
-        f32x2 s = 0ull;
+        f32x2 s[4] = {0ull, 0ull, 0ull, 0ull};  // four independent FMA chains
 #pragma unroll
         for (int j = 0; j < C::VPB; ++j) {
             const uint4 v =
@@ -173,11 +173,11 @@ __device__ __forceinline__ float block_dot(const uint8_t *ws, const float *xb, i
                 f32x2 p[2];
                 i8_word(word_of(v, t), mg, p);
                 const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xb + j * 16 + 4 * t);
-                s = fma2(p[0], xa.x, s);
-                s = fma2(p[1], xa.y, s);
+                s[t] = fma2(p[0], xa.x, s[t]);
+                s[t] = fma2(p[1], xa.y, s[t]);
             }
         }
-        const float2 r = unpack2(s);
+        const float2 r = unpack2(add2(add2(s[0], s[1]), add2(s[2], s[3])));
         return d * (r.x + r.y);
     } else {  // Q6_K super-block: 16 sub-blocks with int8 sub-scales
         const uint8_t *sb = ws + b * C::VPB * kVecBytes + lane * 16;
@@ -195,16 +195,20 @@ __device__ __forceinline__ float block_dot(const uint8_t *ws, const float *xb, i
                 const int sub = 4 * q + u;
                 f32x2 p[8];
                 q6_group(w[3 * u], w[3 * u + 1], w[3 * u + 2], mg, p);
-                f32x2 s = 0ull;
+                f32x2 s0 = 0ull, s1 = 0ull;  // two independent FMA chains
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 4; j += 2) {
                     const ulonglong2 xa =
                         *reinterpret_cast<const ulonglong2 *>(xb + sub * 16 + 4 * j);
-                    s = fma2(p[2 * j], xa.x, s);
-                    s = fma2(p[2 * j + 1], xa.y, s);
+                    const ulonglong2 xc =
+                        *reinterpret_cast<const ulonglong2 *>(xb + sub * 16 + 4 * j + 4);
+                    s0 = fma2(p[2 * j], xa.x, s0);
+                    s0 = fma2(p[2 * j + 1], xa.y, s0);
+                    s1 = fma2(p[2 * j + 2], xc.x, s1);
+                    s1 = fma2(p[2 * j + 3], xc.y, s1);
                 }
                 const float sc = i8_byte(word_of(scv, sub >> 2), sub & 3, mg);
-                const float2 r = unpack2(s);
+                const float2 r = unpack2(add2(s0, s1));
                 acc = fmaf(d * sc, r.x + r.y, acc);
             }
         }
