@@ -185,23 +185,13 @@ lean_status dequant_fmt(const Geom &g, const uint8_t *W, float *w, cudaStream_t 
 
 // -------------------------------------------------------------- stream path ---
 
-// Steps and groups of a problem list; false when the list is too long.
-inline bool stream_totals(const HostProb *ph, int n, int64_t *steps, int64_t *groups) {
+// Total row groups of a problem list; false when the list is too long.
+inline bool stream_totals(const HostProb *ph, int n, int64_t *groups) {
     if (n < 1 || n > kMaxBatch) return false;
-    int64_t t = 0, gg = 0;
-    for (int i = 0; i < n; ++i) {
-        t += ph[i].g.groups * ph[i].g.steps;
-        gg += ph[i].g.groups;
-    }
-    *steps = t;
+    int64_t gg = 0;
+    for (int i = 0; i < n; ++i) gg += ph[i].g.groups;
     *groups = gg;
     return true;
-}
-
-inline int64_t stream_workspace_bytes(const HostProb *ph, int n) {
-    int64_t steps, groups;
-    if (!stream_totals(ph, n, &steps, &groups)) return -1;
-    return workspace_layout(groups).total;
 }
 
 template <int FMT, int NP>
@@ -212,7 +202,8 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
     static std::atomic<uint64_t> smem_done{0};
     StreamArgs<NP> a;
     a.nprob = n;
-    int64_t steps = 0, groups = 0;
+    a.pad = 0;
+    int64_t units = 0, gblocks = 0, groups = 0;
     for (int i = 0; i < n; ++i) {
         const Geom &g = ph[i].g;
         StreamProb &p = a.p[i];
@@ -223,28 +214,33 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
         p.K = (int)g.K;
         p.steps = g.steps;
         p.last_blocks = g.last_blocks;
+        p.chunks = (g.steps - 1) * L::CPSTEP + (g.last_blocks + C::BPC - 1) / C::BPC;
+        p.pad = 0;
         p.group_vecs = g.group_vecs;
         p.groups = g.groups;
-        p.step0 = steps;
+        p.gblocks = (g.groups + kStreamWarps - 1) / kStreamWarps;
+        p.unit0 = units;
+        p.gblock0 = gblocks;
         p.group0 = groups;
-        steps += g.groups * g.steps;
+        units += p.gblocks * p.chunks;
+        gblocks += p.gblocks;
         groups += g.groups;
     }
-    a.total_steps = steps;
-    a.total_groups = groups;
+    a.total_units = units;
+    a.total_gblocks = gblocks;
     a.mg = make_magic();
     a.err = err;
-    const int64_t sms = std::min<int64_t>((int64_t)sm_count() * C::CPS, kMaxStreamCtas);
+    const int64_t slots = std::min<int64_t>((int64_t)sm_count() * C::CPS, kMaxStreamCtas);
     if (ws != nullptr) {
         const WorkspaceLayout wl = workspace_layout(groups);
         if (ws_bytes < wl.total) return LEAN_ERR_SHAPE;
         a.balanced = 1;
-        a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(sms, (steps + C::KS - 1) / C::KS));
+        a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, units));
         a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + wl.part_off);
         a.cnt = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + wl.cnt_off);
     } else {
         a.balanced = 0;
-        a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(sms, groups));
+        a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, gblocks));
         a.part = nullptr;
         a.cnt = nullptr;
     }
@@ -263,8 +259,8 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
 template <int FMT>
 lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
                        unsigned *err, cudaStream_t stream) {
-    int64_t steps, groups;
-    if (!stream_totals(ph, n, &steps, &groups)) return LEAN_ERR_SHAPE;
+    int64_t groups;
+    if (!stream_totals(ph, n, &groups)) return LEAN_ERR_SHAPE;
     if (n == 1) return launch_stream<FMT, 1>(ph, n, flags, ws, ws_bytes, err, stream);
     return launch_stream<FMT, kMaxBatch>(ph, n, flags, ws, ws_bytes, err, stream);
 }

@@ -4,27 +4,29 @@
 // is memory-bandwidth bound, each generated token streams all dense weights
 // once), so this kernel is a pipeline whose only job is to keep HBM busy:
 //
-//  - one producer lane per CTA copies whole steps (8 blocks of one 32-row
-//    group: their quant vectors and scale vector, contiguous in the packed
-//    layout) plus the matching slice of x into a ring of shared-memory slots
-//    with bulk asynchronous copies (cp.async.bulk, completion counted in bytes
-//    on an mbarrier per slot);
-//  - eight consumer warps decode the slot from shared memory (lane r owns row
-//    r of the group: conflict-free 16-byte reads; x is a broadcast read) and
-//    accumulate in fp32, then release the slot on a second mbarrier;
-//  - a CTA works on a contiguous range of the flattened (problem, row group,
-//    step) list.  Without a workspace the ranges are whole row groups; with a
-//    workspace they are equal numbers of steps (stream-K), and a group split
-//    between CTAs is completed by the last CTA to arrive, which adds the
+//  - work is cut into units: one chunk of K (BPC blocks of one step) for each
+//    of 8 consecutive 32-row groups of one matrix.  A producer lane copies a
+//    unit -- the 8 groups' quant vectors of the chunk with their scale vector,
+//    and the chunk's slice of x once for all 8 -- into a shared-memory slot
+//    with bulk asynchronous copies (cp.async.bulk), counting the bytes on the
+//    slot's mbarrier;
+//  - consumer warp w owns group w of every unit: lane r decodes row r from
+//    shared memory (conflict-free 16-byte reads, x as a broadcast read) and
+//    keeps the group's running sum in a register across units, so no warp
+//    ever waits for another; the slot is released on a second mbarrier;
+//  - a CTA works on a contiguous range of the flattened (problem, group
+//    block, chunk) list.  Without a workspace the ranges hold whole group
+//    blocks; with one they hold equal numbers of units (stream-K) and a group
+//    split between CTAs is completed by the last CTA to arrive, which adds the
 //    parts in CTA order: results are deterministic either way;
-//  - weights are requested before griddepcontrol.wait, x after it, so with
+//  - weights are requested before griddepcontrol.wait and x after it, so with
 //    programmatic dependent launch the weight stream of one product overlaps
 //    the tail of the previous kernel on the stream;
 //  - every wait is bounded (globaltimer); on timeout the kernel records an
 //    error code, lets its own copies land and returns.
 //
 // Several independent products (same format, M = 1) can share one launch: the
-// list of problems is a kernel parameter, and their steps are concatenated.
+// list of problems is a kernel parameter and their units are concatenated.
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -35,7 +37,7 @@
 
 namespace lean {
 
-constexpr int kStreamWarps = 8;                          // consumer warps per CTA
+constexpr int kStreamWarps = 8;                          // consumer warps = groups per unit
 constexpr int kStreamThreads = 32 * (kStreamWarps + 1);  // + one producer warp
 constexpr uint64_t kWaitLimitNs = 2000000000ull;        // 2 s
 
@@ -50,97 +52,116 @@ struct StreamProb {
     float *y;
     int N, K;
     int steps, last_blocks;  // steps per group, blocks in a group's last step
+    int chunks;              // chunks per group
+    int pad;
     int64_t group_vecs;      // vectors per row group
     int64_t groups;          // row groups
-    int64_t step0, group0;   // first global step / group of this problem
+    int64_t gblocks;         // group blocks (8 groups each)
+    int64_t unit0, gblock0;  // first global unit / group block of this problem
+    int64_t group0;          // first global group
 };
 
 template <int NP>
 struct StreamArgs {
     int nprob;
     int ctas;
-    int balanced;  // 1: equal steps per CTA (needs part/cnt); 0: whole groups per CTA
-    int64_t total_steps, total_groups;
-    float *part;    // [ctas][2][32] partial sums of groups split between CTAs
-    unsigned *cnt;  // [total_groups] arrival counters, all zero between calls
+    int balanced;  // 1: equal units per CTA (needs part/cnt); 0: whole group blocks
+    int pad;
+    int64_t total_units, total_gblocks;
+    float *part;    // [ctas][2][8][32] partial sums of groups split between CTAs
+    unsigned *cnt;  // [total groups] arrival counters, all zero between calls
     unsigned *err;  // device error word (bits of StreamError)
     Magic mg;
     StreamProb p[NP];
 };
 
 template <int FMT> struct StreamCfg;
-// VPB: quant vectors per block; SE: x elements per step; KS: steps per slot;
-// S: slots in the ring; CPS: CTAs per SM.  Each consumer warp handles BPW
-// blocks of one step per slot (128 or 256 weights per lane); an SM holds
-// about 90-190 KB of ring in all.
-template <> struct StreamCfg<Q4_0> { static constexpr int VPB = 1, SE = 256, KS = 8, S = 2, CPS = 2; };
-template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, SE = 256, KS = 4, S = 2, CPS = 2; };
-template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, SE = 512, KS = 2, S = 2, CPS = 2; };
-template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, SE = 2048, KS = 1, S = 3, CPS = 1; };
+// VPB: quant vectors per block; BPC: blocks per chunk; E: weights per block;
+// S: slots in the ring; CPS: CTAs per SM.  A unit is 8 x BPC blocks of 32
+// rows plus x: about 37 KB (Q6_K 58 KB).
+template <> struct StreamCfg<Q4_0> { static constexpr int VPB = 1, BPC = 8, E = 32, S = 2, CPS = 2; };
+template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, BPC = 4, E = 32, S = 2, CPS = 2; };
+template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, BPC = 2, E = 64, S = 2, CPS = 2; };
+template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, BPC = 1, E = 256, S = 3, CPS = 1; };
 
 template <int FMT>
 struct StreamLayout {
     using C = StreamCfg<FMT>;
-    static constexpr int STEP_WBYTES = (8 * C::VPB + 1) * kVecBytes;
-    static constexpr int STEP_XBYTES = C::SE * 4;
-    static constexpr int STEP_BYTES = STEP_WBYTES + STEP_XBYTES;
-    static constexpr int SLOT_BYTES = C::KS * STEP_BYTES;
-    static constexpr int WPS = kStreamWarps / C::KS;  // warps per step
-    static constexpr int BPW = 8 / WPS;               // blocks per warp
-    // shared memory: [full S][empty S][meta S*KS][stage 2*W*32][carry 2*32][abort][ring S*SLOT]
+    static constexpr int CPSTEP = 8 / C::BPC;                          // chunks of a full step
+    static constexpr int CHUNK_BYTES = (C::BPC * C::VPB + 1) * kVecBytes;  // one group's chunk
+    static constexpr int XE = C::BPC * C::E;                           // x elements of a unit
+    static constexpr int SLOT_BYTES = kStreamWarps * CHUNK_BYTES + XE * 4;
+    // shared memory: [full S][empty S][abort][pad][ring S*SLOT]
     static constexpr int OFF_FULL = 0;
     static constexpr int OFF_EMPTY = 8 * C::S;
-    static constexpr int OFF_META = 16 * C::S;
-    static constexpr int OFF_STAGE = OFF_META + 48 * C::S * C::KS;
-    static constexpr int OFF_CARRY = OFF_STAGE + 4 * 2 * kStreamWarps * 32;
-    static constexpr int OFF_ABORT = OFF_CARRY + 4 * 2 * 32;
-    static constexpr int OFF_RING = (OFF_ABORT + 16 + 127) / 128 * 128;
+    static constexpr int OFF_ABORT = 16 * C::S;
+    static constexpr int OFF_RING = 128;
     static constexpr int SMEM = OFF_RING + C::S * SLOT_BYTES;
+    static_assert(OFF_ABORT + 4 <= OFF_RING, "barriers fit before the ring");
 };
 
 __device__ __forceinline__ int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }
 __device__ __forceinline__ int64_t i64max(int64_t a, int64_t b) { return a > b ? a : b; }
 
 template <int NP>
-__device__ __forceinline__ int find_prob_by_step(const StreamArgs<NP> &a, int64_t t) {
+__device__ __forceinline__ int find_prob_by_unit(const StreamArgs<NP> &a, int64_t u) {
     int lo = 0, hi = a.nprob - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.p[mid].step0 <= t) lo = mid; else hi = mid - 1;
+        if (a.p[mid].unit0 <= u) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
 template <int NP>
-__device__ __forceinline__ int find_prob_by_group(const StreamArgs<NP> &a, int64_t g) {
+__device__ __forceinline__ int find_prob_by_gblock(const StreamArgs<NP> &a, int64_t gb) {
     int lo = 0, hi = a.nprob - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.p[mid].group0 <= g) lo = mid; else hi = mid - 1;
+        if (a.p[mid].gblock0 <= gb) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
-// first global step of global group g (g == total_groups gives total_steps)
+// first global unit of global group block gb (gb == total_gblocks gives total_units)
 template <int NP>
-__device__ __forceinline__ int64_t group_first_step(const StreamArgs<NP> &a, int64_t g) {
-    if (g >= a.total_groups) return a.total_steps;
-    const StreamProb &p = a.p[find_prob_by_group(a, g)];
-    return p.step0 + (g - p.group0) * p.steps;
+__device__ __forceinline__ int64_t gblock_first_unit(const StreamArgs<NP> &a, int64_t gb) {
+    if (gb >= a.total_gblocks) return a.total_units;
+    const StreamProb &p = a.p[find_prob_by_gblock(a, gb)];
+    return p.unit0 + (gb - p.gblock0) * p.chunks;
 }
 template <int NP>
 __device__ __forceinline__ int64_t range_begin(const StreamArgs<NP> &a, int64_t i) {
-    if (a.balanced) return a.total_steps * i / a.ctas;
-    return group_first_step(a, a.total_groups * i / a.ctas);
+    if (a.balanced) return a.total_units * i / a.ctas;
+    return gblock_first_unit(a, a.total_gblocks * i / a.ctas);
 }
-// the CTA whose balanced range holds step t
+// the CTA whose balanced range holds unit u
 template <int NP>
-__device__ __forceinline__ int64_t cta_of_step(const StreamArgs<NP> &a, int64_t t) {
-    int64_t i = t * a.ctas / a.total_steps;
-    while (i + 1 < a.ctas && a.total_steps * (i + 1) / a.ctas <= t) ++i;
-    while (i > 0 && a.total_steps * i / a.ctas > t) --i;
+__device__ __forceinline__ int64_t cta_of_unit(const StreamArgs<NP> &a, int64_t u) {
+    int64_t i = u * a.ctas / a.total_units;
+    while (i + 1 < a.ctas && a.total_units * (i + 1) / a.ctas <= u) ++i;
+    while (i > 0 && a.total_units * i / a.ctas > u) --i;
     return i;
 }
 
-// ---- per-format consumer work on one step held in shared memory -------------
+// Where a unit's chunk sits in its groups' streams.
+struct ChunkPos {
+    int s;     // step
+    int sub;   // chunk inside the step
+    int nblk;  // blocks of the step
+    int nbc;   // blocks of the chunk
+};
+template <int FMT>
+__device__ __forceinline__ ChunkPos chunk_pos(const StreamProb &p, int c) {
+    using C = StreamCfg<FMT>;
+    constexpr int CPSTEP = StreamLayout<FMT>::CPSTEP;
+    ChunkPos q;
+    q.s = c / CPSTEP;
+    q.sub = c % CPSTEP;
+    q.nblk = q.s == p.steps - 1 ? p.last_blocks : 8;
+    q.nbc = min(C::BPC, q.nblk - q.sub * C::BPC);
+    return q;
+}
+
+// ---- per-format consumer work on one chunk held in shared memory ------------
 // One block: this lane's row, block b of the step at ws, x of the block at xb.
 template <int FMT>
 __device__ __forceinline__ float block_dot(const uint8_t *ws, const float *xb, int b, float d,
@@ -216,81 +237,28 @@ __device__ __forceinline__ float block_dot(const uint8_t *ws, const float *xb, i
     }
 }
 
-// This warp's share of sum_k w x for its lane's row: blocks [B0, B0+BPW) of a
-// step with nblk blocks.  B0 is a compile-time constant so that every shared
-// address below is a constant offset; full steps take the unchecked path.
-template <int FMT, int B0>
-__device__ __forceinline__ float consume_step(const uint8_t *ws, const float *xs, int nblk,
-                                              int lane, const Magic &mg) {
+// This lane's row: sum over the chunk's blocks of w * x.  ws: the group's
+// chunk (nbc blocks of quant vectors, then the step's scale vector); xs: the
+// chunk's x; sub: the chunk's place in its step (for the scale slots).
+template <int FMT>
+__device__ __forceinline__ float consume_chunk(const uint8_t *ws, const float *xs, int nbc, int sub,
+                                               int lane, const Magic &mg) {
     using C = StreamCfg<FMT>;
-    constexpr int BPW = StreamLayout<FMT>::BPW;
+    const uint4 sv = *reinterpret_cast<const uint4 *>(ws + nbc * C::VPB * kVecBytes + lane * 16);
     float acc = 0.f;
-    if (nblk == 8) {
-        const uint4 sv =
-            *reinterpret_cast<const uint4 *>(ws + 8 * C::VPB * kVecBytes + lane * 16);
+    if (nbc == C::BPC) {
 #pragma unroll
-        for (int i = 0; i < BPW; ++i)
-            acc += block_dot<FMT>(ws, xs + (B0 + i) * (C::SE / 8), B0 + i, scale_of(sv, B0 + i),
-                                  lane, mg);
+        for (int i = 0; i < C::BPC; ++i)
+            acc += block_dot<FMT>(ws, xs + i * C::E, i, scale_of(sv, sub * C::BPC + i), lane, mg);
     } else {
-        const uint4 sv =
-            *reinterpret_cast<const uint4 *>(ws + nblk * C::VPB * kVecBytes + lane * 16);
 #pragma unroll
-        for (int i = 0; i < BPW; ++i)
-            if (B0 + i < nblk)
-                acc += block_dot<FMT>(ws, xs + (B0 + i) * (C::SE / 8), B0 + i,
-                                      scale_of(sv, B0 + i), lane, mg);
+        for (int i = 0; i < C::BPC; ++i)
+            if (i < nbc)
+                acc += block_dot<FMT>(ws, xs + i * C::E, i, scale_of(sv, sub * C::BPC + i), lane,
+                                      mg);
     }
     return acc;
 }
-
-// This warp's share with a runtime first block (one code copy for all warps).
-template <int FMT>
-__device__ __forceinline__ float consume_any(const uint8_t *ws, const float *xs, int nblk, int b0,
-                                             int lane, const Magic &mg) {
-    using C = StreamCfg<FMT>;
-    constexpr int BPW = StreamLayout<FMT>::BPW;
-    const uint4 sv = *reinterpret_cast<const uint4 *>(ws + nblk * C::VPB * kVecBytes + lane * 16);
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < BPW; ++i) {
-        const int b = b0 + i;
-        if (b < nblk) acc += block_dot<FMT>(ws, xs + b * (C::SE / 8), b, scale_of(sv, b), lane, mg);
-    }
-    return acc;
-}
-
-// dispatch on the warp's (runtime) first block: compile-time offsets when a
-// step is split over at most two warps, a single code copy otherwise
-template <int FMT>
-__device__ __forceinline__ float consume(const uint8_t *ws, const float *xs, int nblk, int b0,
-                                         int lane, const Magic &mg) {
-    constexpr int BPW = StreamLayout<FMT>::BPW;
-    if (8 / BPW > 2) return consume_any<FMT>(ws, xs, nblk, b0, lane, mg);
-    switch (b0 / BPW) {
-    case 0: return consume_step<FMT, 0>(ws, xs, nblk, lane, mg);
-    case 1: if (BPW * 1 < 8) return consume_step<FMT, (BPW * 1) % 8>(ws, xs, nblk, lane, mg); break;
-    case 2: if (BPW * 2 < 8) return consume_step<FMT, (BPW * 2) % 8>(ws, xs, nblk, lane, mg); break;
-    case 3: if (BPW * 3 < 8) return consume_step<FMT, (BPW * 3) % 8>(ws, xs, nblk, lane, mg); break;
-    case 4: if (BPW * 4 < 8) return consume_step<FMT, (BPW * 4) % 8>(ws, xs, nblk, lane, mg); break;
-    case 5: if (BPW * 5 < 8) return consume_step<FMT, (BPW * 5) % 8>(ws, xs, nblk, lane, mg); break;
-    case 6: if (BPW * 6 < 8) return consume_step<FMT, (BPW * 6) % 8>(ws, xs, nblk, lane, mg); break;
-    case 7: if (BPW * 7 < 8) return consume_step<FMT, (BPW * 7) % 8>(ws, xs, nblk, lane, mg); break;
-    }
-    return 0.f;
-}
-
-// What the producer learned about one step of a slot, for the consumers.
-struct StepMeta {
-    int64_t g;       // global row group
-    int64_t gs, ge;  // global step range of that group
-    const float *x;  // x slice copied for the step
-    int pi;          // problem index
-    int nblk;        // blocks in the step
-    int xe;          // x elements copied
-    int step;        // step inside the group
-};
-static_assert(sizeof(StepMeta) == 48, "StepMeta layout");
 
 template <int FMT, int NP>
 __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
@@ -301,17 +269,13 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     extern __shared__ __align__(128) uint8_t sbuf[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sbuf + L::OFF_FULL);
     uint64_t *empty = reinterpret_cast<uint64_t *>(sbuf + L::OFF_EMPTY);
-    StepMeta *meta = reinterpret_cast<StepMeta *>(sbuf + L::OFF_META);
-    float *stage = reinterpret_cast<float *>(sbuf + L::OFF_STAGE);   // [2][W][32]
-    float *carry = reinterpret_cast<float *>(sbuf + L::OFF_CARRY);   // [2][32]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbuf + L::OFF_ABORT);
     uint8_t *ring = sbuf + L::OFF_RING;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t cta = blockIdx.x;
     const int64_t beg = range_begin(a, cta), end = range_begin(a, cta + 1);
-    const int64_t nsteps = end - beg;
-    const int64_t nslots = (nsteps + C::KS - 1) / C::KS;
+    const int64_t nunits = end - beg;
 
     // Let the next kernel on the stream start streaming its own weights.
     pdl_launch_dependents();
@@ -321,74 +285,72 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kStreamWarps);
         }
-        fence_mbar_init();
         *abort_flag = 0;
+        fence_mbar_init();
     }
     __syncthreads();
-    if (nsteps <= 0) return;
+    if (nunits <= 0) return;
+
+    // cursor over the CTA's units: problem, group block inside it, chunk
+    int pi = find_prob_by_unit(a, beg);
+    int64_t gb;
+    int c;
+    {
+        const int64_t o = beg - a.p[pi].unit0;
+        gb = o / a.p[pi].chunks;
+        c = (int)(o % a.p[pi].chunks);
+    }
+    auto advance = [&]() {
+        if (++c == a.p[pi].chunks) {
+            c = 0;
+            if (++gb == a.p[pi].gblocks) {
+                gb = 0;
+                ++pi;
+            }
+        }
+    };
 
     if (warp == kStreamWarps) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        // cursor over the CTA's steps: problem, group inside it, step inside the group
-        int pi = find_prob_by_step(a, beg);
-        int64_t g, s;
-        {
-            const int64_t o = beg - a.p[pi].step0;
-            g = o / a.p[pi].steps;
-            s = o % a.p[pi].steps;
-        }
-        // fill the metadata of slot j, arm its barrier and copy its weights
-        auto issue_weights = [&](int64_t j) {
+        const float *xsrc[C::S];
+        uint32_t xbytes[C::S];
+        // arm slot j's barrier for the whole unit and copy the weights; returns
+        // the x source through xs / xb for a later copy
+        auto issue_weights = [&](int64_t j, const float *&xs, uint32_t &xb) {
             const int sl = (int)(j % C::S);
-            const int ns = (int)i64min(C::KS, nsteps - j * C::KS);
             uint8_t *base = ring + sl * L::SLOT_BYTES;
-            StepMeta *m = meta + sl * C::KS;
-            uint32_t bytes = 0;
-            for (int i = 0; i < ns; ++i) {
-                const StreamProb &p = a.p[pi];
-                const int nblk = s == p.steps - 1 ? p.last_blocks : 8;
-                const int xe = min(C::SE, p.K - (int)s * C::SE);
-                m[i].g = p.group0 + g;
-                m[i].gs = p.step0 + g * p.steps;
-                m[i].ge = m[i].gs + p.steps;
-                m[i].x = p.x + s * C::SE;
-                m[i].pi = pi;
-                m[i].nblk = nblk;
-                m[i].xe = xe;
-                m[i].step = (int)s;
-                bytes += (nblk * C::VPB + 1) * kVecBytes + xe * 4;
-                if (++s == p.steps) {  // advance the cursor
-                    s = 0;
-                    if (++g == p.groups) {
-                        g = 0;
-                        ++pi;
-                    }
+            const StreamProb &p = a.p[pi];
+            const ChunkPos q = chunk_pos<FMT>(p, c);
+            const int ng = (int)i64min(kStreamWarps, p.groups - gb * kStreamWarps);
+            const uint32_t qbytes = q.nbc * C::VPB * kVecBytes;
+            xb = q.nbc * C::E * 4;
+            xs = p.x + (int64_t)(q.s * 8 + q.sub * C::BPC) * C::E;
+            mbar_arrive_expect_tx(&full[sl], ng * (qbytes + kVecBytes) + xb);
+            const bool merged = q.sub * C::BPC + q.nbc == q.nblk;  // chunk ends at the scale vector
+            for (int w = 0; w < ng; ++w) {
+                const uint8_t *step =
+                    p.W + ((gb * kStreamWarps + w) * p.group_vecs + (int64_t)q.s * SV) * kVecBytes;
+                uint8_t *dst = base + w * L::CHUNK_BYTES;
+                const uint8_t *qsrc = step + q.sub * C::BPC * C::VPB * kVecBytes;
+                if (merged) {
+                    bulk_g2s(dst, qsrc, qbytes + kVecBytes, &full[sl]);
+                } else {
+                    bulk_g2s(dst, qsrc, qbytes, &full[sl]);
+                    bulk_g2s(dst + qbytes, step + q.nblk * C::VPB * kVecBytes, kVecBytes, &full[sl]);
                 }
             }
-            mbar_arrive_expect_tx(&full[sl], bytes);  // releases the metadata too
-            for (int i = 0; i < ns; ++i) {
-                const StreamProb &p = a.p[m[i].pi];
-                const int64_t lg = m[i].g - p.group0;
-                const uint8_t *src =
-                    p.W + (lg * p.group_vecs + (int64_t)m[i].step * SV) * kVecBytes;
-                bulk_g2s(base + i * L::STEP_BYTES, src, (m[i].nblk * C::VPB + 1) * kVecBytes,
-                         &full[sl]);
-            }
+            advance();
         };
-        auto issue_x = [&](int64_t j) {
+        auto issue_x = [&](int64_t j, const float *xs, uint32_t xb) {
             const int sl = (int)(j % C::S);
-            const int ns = (int)i64min(C::KS, nsteps - j * C::KS);
-            uint8_t *base = ring + sl * L::SLOT_BYTES;
-            const StepMeta *m = meta + sl * C::KS;
-            for (int i = 0; i < ns; ++i)
-                bulk_g2s(base + i * L::STEP_BYTES + L::STEP_WBYTES, m[i].x, m[i].xe * 4, &full[sl]);
+            bulk_g2s(ring + sl * L::SLOT_BYTES + kStreamWarps * L::CHUNK_BYTES, xs, xb, &full[sl]);
         };
-        const int64_t nfill = i64min(C::S, nslots);
-        for (int64_t j = 0; j < nfill; ++j) issue_weights(j);
+        const int64_t nfill = i64min(C::S, nunits);
+        for (int64_t j = 0; j < nfill; ++j) issue_weights(j, xsrc[j], xbytes[j]);
         pdl_wait();  // x may be written by the previous kernel on the stream
-        for (int64_t j = 0; j < nfill; ++j) issue_x(j);
-        for (int64_t j = nfill; j < nslots; ++j) {
+        for (int64_t j = 0; j < nfill; ++j) issue_x(j, xsrc[j], xbytes[j]);
+        for (int64_t j = nfill; j < nunits; ++j) {
             const int sl = (int)(j % C::S);
             if (*abort_flag || !mbar_wait(&empty[sl], (uint32_t)((j / C::S - 1) & 1), kWaitLimitNs)) {
                 atomicOr(a.err, kErrEmptyTimeout);
@@ -397,98 +359,75 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
                     mbar_wait(&full[k % C::S], (uint32_t)((k / C::S) & 1), kWaitLimitNs);
                 return;
             }
-            issue_weights(j);
-            issue_x(j);
+            const float *xs;
+            uint32_t xb;
+            issue_weights(j, xs, xb);
+            issue_x(j, xs, xb);
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    // Each warp computes its blocks of one step per slot and stages its sum;
-    // after a barrier of the consumer warps, warp r adds up run r of the slot
-    // (consecutive steps of one row group) in step order, carrying a group
-    // that continues into the next slot.  A group complete in this CTA is
-    // stored; one shared with other CTAs (workspace mode) is published and
-    // finished by the last CTA.  Every sum is taken in a fixed order.
-    const int si = warp / L::WPS;             // step of the slot this warp works on
-    const int b0 = (warp % L::WPS) * L::BPW;  // its first block in that step
+    // Warp w owns group w of each unit and keeps its sum in `acc` until the
+    // group's last chunk in this CTA.  A group complete in the CTA is stored;
+    // one shared with other CTAs (workspace mode) is published and finished by
+    // the last CTA to arrive.
     const Magic mg = pin(a.mg);
-
-    // finish the CTA's part of group g (global steps [gs, ge), problem pi) with value v
-    auto finish_group = [&](int64_t g, int64_t gs, int64_t ge, int pi, float v) {
-        const StreamProb &p = a.p[pi];
-        const int64_t n = (g - p.group0) * kRowsPerGroup + lane;
-        if (gs >= beg && ge <= end) {  // the whole group is in this CTA
-            if (n < p.N) p.y[n] = v;
+    float acc = 0.f;
+    for (int64_t j = 0; j < nunits; ++j) {
+        const int sl = (int)(j % C::S);
+        if (!mbar_wait(&full[sl], (uint32_t)((j / C::S) & 1), kWaitLimitNs)) {
+            if (lane == 0) {
+                atomicOr(a.err, kErrFullTimeout);
+                *abort_flag = 1;
+            }
             return;
         }
-        // group split between CTAs: publish, the last CTA to arrive adds up
-        const int side = gs < beg ? 0 : 1;
-        a.part[(cta * 2 + side) * 32 + lane] = v;
-        __threadfence();
+        const StreamProb &p = a.p[pi];
+        const int64_t g = gb * kStreamWarps + warp;  // this warp's group in the problem
+        const bool live = g < p.groups;
+        if (live) {
+            const ChunkPos q = chunk_pos<FMT>(p, c);
+            const uint8_t *ws = ring + sl * L::SLOT_BYTES + warp * L::CHUNK_BYTES;
+            const float *xs =
+                reinterpret_cast<const float *>(ring + sl * L::SLOT_BYTES + kStreamWarps * L::CHUNK_BYTES);
+            acc += consume_chunk<FMT>(ws, xs, q.nbc, q.sub, lane, mg);
+        }
         __syncwarp();
-        unsigned arrived = 0;
-        if (lane == 0) arrived = atomicAdd(&a.cnt[g], 1u);
-        arrived = __shfl_sync(0xffffffffu, arrived, 0);
-        const int64_t i0 = cta_of_step(a, gs), i1 = cta_of_step(a, ge - 1);
-        if (arrived + 1 != (unsigned)(i1 - i0 + 1)) return;
-        __threadfence();
-        float tot = 0.f;
-        for (int64_t i = i0; i <= i1; ++i) {
-            const int sd = (i == i0) ? 1 : 0;
-            tot += __ldcg(&a.part[(i * 2 + sd) * 32 + lane]);
-        }
-        if (n < p.N) p.y[n] = tot;
-        if (lane == 0) a.cnt[g] = 0;  // ready for the next call
-    };
-
-    for (int64_t j = 0; j < nslots; ++j) {
-        const int sl = (int)(j % C::S);
-        const int ns = (int)i64min(C::KS, nsteps - j * C::KS);
-        const bool ok = mbar_wait(&full[sl], (uint32_t)((j / C::S) & 1), kWaitLimitNs);
-        if (!ok && lane == 0) {
-            atomicOr(a.err, kErrFullTimeout);
-            *abort_flag = 1;
-        }
-        float v = 0.f;
-        if (ok && si < ns) {
-            const StepMeta &m = meta[sl * C::KS + si];
-            const uint8_t *ws = ring + sl * L::SLOT_BYTES + si * L::STEP_BYTES;
-            const float *xs = reinterpret_cast<const float *>(ws + L::STEP_WBYTES);
-            v = consume<FMT>(ws, xs, m.nblk, b0, lane, mg);
-        }
-        float *stg = stage + (j & 1) * kStreamWarps * 32;
-        stg[warp * 32 + lane] = v;
-        named_barrier_sync(1, 32 * kStreamWarps);  // every consumer warp staged its sum
-        // all consumer warps read the flag after the same barrier: they stop together
-        if (*abort_flag) return;
-        {
-            // run r of the slot: the r-th maximal run of steps with one group
-            const StepMeta *m = meta + sl * C::KS;
-            int r = 0, i0 = 0;
-            for (int i = 1; i <= ns && r <= warp; ++i) {
-                if (i == ns || m[i].g != m[i0].g) {
-                    if (r == warp) {
-                        const StepMeta &mm = m[i0];
-                        float sum = 0.f;
-                        const int64_t t0 = beg + j * C::KS + i0;
-                        if (t0 != mm.gs && t0 != beg)  // continues a run of the previous slot
-                            sum = carry[((j + 1) & 1) * 32 + lane];
-                        for (int k = i0 * L::WPS; k < i * L::WPS; ++k) sum += stg[k * 32 + lane];
-                        const int64_t t1 = beg + j * C::KS + i;  // one past the run
-                        if (t1 == i64min(mm.ge, end)) {
-                            finish_group(mm.g, mm.gs, mm.ge, mm.pi, sum);
-                        } else {  // the group goes on in the next slot
-                            carry[(j & 1) * 32 + lane] = sum;
-                        }
+        if (lane == 0) mbar_arrive(&empty[sl]);  // the slot is free; the sum is in registers
+        const bool group_done = c == p.chunks - 1;
+        if (live && (group_done || j == nunits - 1)) {
+            const int64_t u0 = p.unit0 + gb * p.chunks;  // the group's first and last unit
+            const int64_t u1 = u0 + p.chunks - 1;
+            const int64_t n = g * kRowsPerGroup + lane;
+            if (u0 >= beg && u1 < end) {  // the whole group is in this CTA
+                if (n < p.N) p.y[n] = acc;
+            } else {
+                // split between CTAs: publish; the last CTA to arrive adds up
+                const int side = u0 < beg ? 0 : 1;
+                a.part[((cta * 2 + side) * kStreamWarps + warp) * 32 + lane] = acc;
+                __threadfence();
+                __syncwarp();
+                const int64_t gg = p.group0 + g;
+                unsigned arrived = 0;
+                if (lane == 0) arrived = atomicAdd(&a.cnt[gg], 1u);
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                const int64_t i0 = cta_of_unit(a, u0), i1 = cta_of_unit(a, u1);
+                if (arrived + 1 == (unsigned)(i1 - i0 + 1)) {
+                    __threadfence();
+                    float tot = 0.f;
+                    for (int64_t i = i0; i <= i1; ++i) {
+                        const int sd = (i == i0) ? 1 : 0;
+                        tot += __ldcg(&a.part[((i * 2 + sd) * kStreamWarps + warp) * 32 + lane]);
                     }
-                    ++r;
-                    i0 = i;
+                    if (n < p.N) p.y[n] = tot;
+                    if (lane == 0) a.cnt[gg] = 0;  // ready for the next call
                 }
             }
+            acc = 0.f;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[sl]);
+        if (group_done) acc = 0.f;
+        advance();
     }
 }
 

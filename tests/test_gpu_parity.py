@@ -237,7 +237,7 @@ def test_workspace_split_groups(lean, fmt, N, nblk):
         outs.append(y)
     assert np.array_equal(outs[0], outs[1])
     # the counters region must be back to zero
-    cnt_off = 512 * 2 * 32 * 4
+    cnt_off = 512 * 2 * 8 * 32 * 4
     assert int(ws[cnt_off:].count_nonzero()) == 0
     assert lean.lean_device_error(True) == 0
 
