@@ -21,7 +21,7 @@ struct HostProb {
 };
 
 // Workspace of the balanced (stream-K) GEMV: per-CTA partial sums of the row
-// groups split between CTAs (two sides x 8 groups x 32 rows), then one
+// groups split between CTAs (two sides x 16 groups x 32 rows), then one
 // arrival counter per row group.
 struct WorkspaceLayout {
     int64_t part_off, cnt_off, total;
@@ -29,7 +29,7 @@ struct WorkspaceLayout {
 inline WorkspaceLayout workspace_layout(int64_t groups) {
     WorkspaceLayout w;
     w.part_off = 0;
-    w.cnt_off = (int64_t)kMaxStreamCtas * 2 * 8 * 32 * 4;
+    w.cnt_off = (int64_t)kMaxStreamCtas * 2 * 16 * 32 * 4;
     w.total = (w.cnt_off + groups * 4 + 255) / 256 * 256;
     return w;
 }

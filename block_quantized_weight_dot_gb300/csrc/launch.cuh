@@ -218,7 +218,7 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
         p.pad = 0;
         p.group_vecs = g.group_vecs;
         p.groups = g.groups;
-        p.gblocks = (g.groups + kStreamWarps - 1) / kStreamWarps;
+        p.gblocks = (g.groups + L::GPU - 1) / L::GPU;
         p.unit0 = units;
         p.gblock0 = gblocks;
         p.group0 = groups;

@@ -37,7 +37,8 @@
 
 namespace lean {
 
-constexpr int kStreamWarps = 8;                          // consumer warps = groups per unit
+constexpr int kStreamWarps = 8;                          // consumer warps per CTA
+constexpr int kMaxGroupsPerUnit = 16;                    // workspace slots per CTA side
 constexpr int kStreamThreads = 32 * (kStreamWarps + 1);  // + one producer warp
 constexpr uint64_t kWaitLimitNs = 2000000000ull;        // 2 s
 
@@ -79,10 +80,26 @@ template <int FMT> struct StreamCfg;
 // VPB: quant vectors per block; BPC: blocks per chunk; E: weights per block;
 // S: slots in the ring; CPS: CTAs per SM.  A unit is 8 x BPC blocks of 32
 // rows plus x: about 37 KB (Q6_K 58 KB).
-template <> struct StreamCfg<Q4_0> { static constexpr int VPB = 1, BPC = 8, E = 32, S = 2, CPS = 2; };
-template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, BPC = 4, E = 32, S = 2, CPS = 2; };
-template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, BPC = 2, E = 64, S = 2, CPS = 2; };
-template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, BPC = 1, E = 256, S = 3, CPS = 1; };
+// GPW: row groups per consumer warp (the warps share the unit's x reads).
+#ifndef LEAN_Q4_BPC
+#define LEAN_Q4_BPC 8
+#endif
+#ifndef LEAN_Q4_GPW
+#define LEAN_Q4_GPW 1
+#endif
+#ifndef LEAN_Q4_S
+#define LEAN_Q4_S 2
+#endif
+#ifndef LEAN_Q4_CPS
+#define LEAN_Q4_CPS 2
+#endif
+template <> struct StreamCfg<Q4_0> {
+    static constexpr int VPB = 1, BPC = LEAN_Q4_BPC, E = 32, S = LEAN_Q4_S, CPS = LEAN_Q4_CPS,
+                         GPW = LEAN_Q4_GPW;
+};
+template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, BPC = 4, E = 32, S = 2, CPS = 2, GPW = 1; };
+template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, BPC = 2, E = 64, S = 2, CPS = 2, GPW = 1; };
+template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, BPC = 1, E = 256, S = 3, CPS = 1, GPW = 1; };
 
 template <int FMT>
 struct StreamLayout {
@@ -90,7 +107,8 @@ struct StreamLayout {
     static constexpr int CPSTEP = 8 / C::BPC;                          // chunks of a full step
     static constexpr int CHUNK_BYTES = (C::BPC * C::VPB + 1) * kVecBytes;  // one group's chunk
     static constexpr int XE = C::BPC * C::E;                           // x elements of a unit
-    static constexpr int SLOT_BYTES = kStreamWarps * CHUNK_BYTES + XE * 4;
+    static constexpr int GPU = kStreamWarps * C::GPW;                  // row groups of a unit
+    static constexpr int SLOT_BYTES = GPU * CHUNK_BYTES + XE * 4;
     // shared memory: [full S][empty S][abort][pad][ring S*SLOT]
     static constexpr int OFF_FULL = 0;
     static constexpr int OFF_EMPTY = 8 * C::S;
@@ -260,6 +278,78 @@ __device__ __forceinline__ float consume_chunk(const uint8_t *ws, const float *x
     return acc;
 }
 
+// Q4_0, R row groups sharing each x read: block b of every group's chunk.
+template <int R>
+__device__ __forceinline__ void q4_block_rows(const uint8_t *ws, int stride, const float *xb, int b,
+                                              const float (&d)[R], int lane, const Magic &mg,
+                                              float (&acc)[R]) {
+    uint4 v[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        v[r] = *reinterpret_cast<const uint4 *>(ws + r * stride + b * kVecBytes + lane * 16);
+    f32x2 s[R][4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t);
+        const ulonglong2 xc = *reinterpret_cast<const ulonglong2 *>(xb + 8 * t + 4);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            f32x2 p[4];
+            q4_word(word_of(v[r], t), mg, p);
+            s[r][t] = mul2(p[0], xa.x);
+            s[r][t] = fma2(p[1], xa.y, s[r][t]);
+            s[r][t] = fma2(p[2], xc.x, s[r][t]);
+            s[r][t] = fma2(p[3], xc.y, s[r][t]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float2 q = unpack2(add2(add2(s[r][0], s[r][1]), add2(s[r][2], s[r][3])));
+        acc[r] = fmaf(d[r], q.x + q.y, acc[r]);
+    }
+}
+
+// All of a warp's live groups (nlive of GPW) on one unit: groups sit
+// kStreamWarps chunks apart in the slot.
+template <int FMT>
+__device__ __forceinline__ void consume_rows(const uint8_t *ws, const float *xs, int nbc, int sub,
+                                             int nlive, int lane, const Magic &mg,
+                                             float (&acc)[StreamCfg<FMT>::GPW]) {
+    using C = StreamCfg<FMT>;
+    using L = StreamLayout<FMT>;
+    constexpr int stride = kStreamWarps * L::CHUNK_BYTES;
+    if (FMT == Q4_0 && C::GPW > 1 && nlive == C::GPW) {
+        uint4 sv[C::GPW];
+#pragma unroll
+        for (int r = 0; r < C::GPW; ++r)
+            sv[r] = *reinterpret_cast<const uint4 *>(ws + r * stride + nbc * C::VPB * kVecBytes +
+                                                     lane * 16);
+        if (nbc == C::BPC) {
+#pragma unroll
+            for (int i = 0; i < C::BPC; ++i) {
+                float d[C::GPW];
+#pragma unroll
+                for (int r = 0; r < C::GPW; ++r) d[r] = scale_of(sv[r], sub * C::BPC + i);
+                q4_block_rows<C::GPW>(ws, stride, xs + i * C::E, i, d, lane, mg, acc);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < C::BPC; ++i) {
+                if (i < nbc) {
+                    float d[C::GPW];
+#pragma unroll
+                    for (int r = 0; r < C::GPW; ++r) d[r] = scale_of(sv[r], sub * C::BPC + i);
+                    q4_block_rows<C::GPW>(ws, stride, xs + i * C::E, i, d, lane, mg, acc);
+                }
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int r = 0; r < C::GPW; ++r)
+        if (r < nlive) acc[r] += consume_chunk<FMT>(ws + r * stride, xs, nbc, sub, lane, mg);
+}
+
 template <int FMT, int NP>
 __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     qmm_stream_kernel(const __grid_constant__ StreamArgs<NP> a) {
@@ -322,7 +412,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             uint8_t *base = ring + sl * L::SLOT_BYTES;
             const StreamProb &p = a.p[pi];
             const ChunkPos q = chunk_pos<FMT>(p, c);
-            const int ng = (int)i64min(kStreamWarps, p.groups - gb * kStreamWarps);
+            const int ng = (int)i64min(L::GPU, p.groups - gb * L::GPU);
             const uint32_t qbytes = q.nbc * C::VPB * kVecBytes;
             xb = q.nbc * C::E * 4;
             xs = p.x + (int64_t)(q.s * 8 + q.sub * C::BPC) * C::E;
@@ -330,7 +420,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             const bool merged = q.sub * C::BPC + q.nbc == q.nblk;  // chunk ends at the scale vector
             for (int w = 0; w < ng; ++w) {
                 const uint8_t *step =
-                    p.W + ((gb * kStreamWarps + w) * p.group_vecs + (int64_t)q.s * SV) * kVecBytes;
+                    p.W + ((gb * L::GPU + w) * p.group_vecs + (int64_t)q.s * SV) * kVecBytes;
                 uint8_t *dst = base + w * L::CHUNK_BYTES;
                 const uint8_t *qsrc = step + q.sub * C::BPC * C::VPB * kVecBytes;
                 if (merged) {
@@ -344,7 +434,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
         };
         auto issue_x = [&](int64_t j, const float *xs, uint32_t xb) {
             const int sl = (int)(j % C::S);
-            bulk_g2s(ring + sl * L::SLOT_BYTES + kStreamWarps * L::CHUNK_BYTES, xs, xb, &full[sl]);
+            bulk_g2s(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES, xs, xb, &full[sl]);
         };
         const int64_t nfill = i64min(C::S, nunits);
         for (int64_t j = 0; j < nfill; ++j) issue_weights(j, xsrc[j], xbytes[j]);
@@ -368,12 +458,14 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     }
 
     // ---------------------------------------------------------------- consumers
-    // Warp w owns group w of each unit and keeps its sum in `acc` until the
-    // group's last chunk in this CTA.  A group complete in the CTA is stored;
-    // one shared with other CTAs (workspace mode) is published and finished by
-    // the last CTA to arrive.
+    // Warp w owns groups w, w + 8, ... of each unit and keeps their sums in
+    // registers until a group's last chunk in this CTA.  A group complete in
+    // the CTA is stored; one shared with other CTAs (workspace mode) is
+    // published and finished by the last CTA to arrive.
     const Magic mg = pin(a.mg);
-    float acc = 0.f;
+    float acc[C::GPW];
+#pragma unroll
+    for (int r = 0; r < C::GPW; ++r) acc[r] = 0.f;
     for (int64_t j = 0; j < nunits; ++j) {
         const int sl = (int)(j % C::S);
         if (!mbar_wait(&full[sl], (uint32_t)((j / C::S) & 1), kWaitLimitNs)) {
@@ -384,49 +476,55 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             return;
         }
         const StreamProb &p = a.p[pi];
-        const int64_t g = gb * kStreamWarps + warp;  // this warp's group in the problem
-        const bool live = g < p.groups;
-        if (live) {
+        const int64_t g0 = gb * L::GPU + warp;  // this warp's first group in the problem
+        const int nlive = (int)i64max(0, i64min(C::GPW, (p.groups - g0 + kStreamWarps - 1) / kStreamWarps));
+        if (nlive > 0) {
             const ChunkPos q = chunk_pos<FMT>(p, c);
             const uint8_t *ws = ring + sl * L::SLOT_BYTES + warp * L::CHUNK_BYTES;
             const float *xs =
-                reinterpret_cast<const float *>(ring + sl * L::SLOT_BYTES + kStreamWarps * L::CHUNK_BYTES);
-            acc += consume_chunk<FMT>(ws, xs, q.nbc, q.sub, lane, mg);
+                reinterpret_cast<const float *>(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES);
+            consume_rows<FMT>(ws, xs, q.nbc, q.sub, nlive, lane, mg, acc);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[sl]);  // the slot is free; the sum is in registers
+        if (lane == 0) mbar_arrive(&empty[sl]);  // the slot is free; the sums are in registers
         const bool group_done = c == p.chunks - 1;
-        if (live && (group_done || j == nunits - 1)) {
-            const int64_t u0 = p.unit0 + gb * p.chunks;  // the group's first and last unit
+        if (group_done || j == nunits - 1) {
+            const int64_t u0 = p.unit0 + gb * p.chunks;  // the groups' first and last unit
             const int64_t u1 = u0 + p.chunks - 1;
-            const int64_t n = g * kRowsPerGroup + lane;
-            if (u0 >= beg && u1 < end) {  // the whole group is in this CTA
-                if (n < p.N) p.y[n] = acc;
-            } else {
-                // split between CTAs: publish; the last CTA to arrive adds up
-                const int side = u0 < beg ? 0 : 1;
-                a.part[((cta * 2 + side) * kStreamWarps + warp) * 32 + lane] = acc;
-                __threadfence();
-                __syncwarp();
-                const int64_t gg = p.group0 + g;
-                unsigned arrived = 0;
-                if (lane == 0) arrived = atomicAdd(&a.cnt[gg], 1u);
-                arrived = __shfl_sync(0xffffffffu, arrived, 0);
-                const int64_t i0 = cta_of_unit(a, u0), i1 = cta_of_unit(a, u1);
-                if (arrived + 1 == (unsigned)(i1 - i0 + 1)) {
+#pragma unroll
+            for (int r = 0; r < C::GPW; ++r) {
+                if (r >= nlive) break;
+                const int64_t g = g0 + r * kStreamWarps;
+                const int slot = warp + r * kStreamWarps;  // the group's place in the unit
+                const int64_t n = g * kRowsPerGroup + lane;
+                if (u0 >= beg && u1 < end) {  // the whole group is in this CTA
+                    if (n < p.N) p.y[n] = acc[r];
+                } else {
+                    // split between CTAs: publish; the last CTA to arrive adds up
+                    const int side = u0 < beg ? 0 : 1;
+                    a.part[((cta * 2 + side) * kMaxGroupsPerUnit + slot) * 32 + lane] = acc[r];
                     __threadfence();
-                    float tot = 0.f;
-                    for (int64_t i = i0; i <= i1; ++i) {
-                        const int sd = (i == i0) ? 1 : 0;
-                        tot += __ldcg(&a.part[((i * 2 + sd) * kStreamWarps + warp) * 32 + lane]);
+                    __syncwarp();
+                    const int64_t gg = p.group0 + g;
+                    unsigned arrived = 0;
+                    if (lane == 0) arrived = atomicAdd(&a.cnt[gg], 1u);
+                    arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                    const int64_t i0 = cta_of_unit(a, u0), i1 = cta_of_unit(a, u1);
+                    if (arrived + 1 == (unsigned)(i1 - i0 + 1)) {
+                        __threadfence();
+                        float tot = 0.f;
+                        for (int64_t i = i0; i <= i1; ++i) {
+                            const int sd = (i == i0) ? 1 : 0;
+                            tot += __ldcg(&a.part[((i * 2 + sd) * kMaxGroupsPerUnit + slot) * 32 + lane]);
+                        }
+                        if (n < p.N) p.y[n] = tot;
+                        if (lane == 0) a.cnt[gg] = 0;  // ready for the next call
                     }
-                    if (n < p.N) p.y[n] = tot;
-                    if (lane == 0) a.cnt[gg] = 0;  // ready for the next call
                 }
             }
-            acc = 0.f;
+#pragma unroll
+            for (int r = 0; r < C::GPW; ++r) acc[r] = 0.f;
         }
-        if (group_done) acc = 0.f;
         advance();
     }
 }
