@@ -38,6 +38,8 @@ SIGNATURES = {
     "lean_batch_workspace_bytes": (_i64, [_int, _int, _vp]),
     "lean_qmatmul_batch": (_int, [_int, _int, _vp, ctypes.c_uint, _vp, _i64, _vp]),
     "lean_device_error": (ctypes.c_uint, [_int]),
+    "lean_qmatmul_fixed_ws": (_int, [_int, _vp, _vp, _vp, _i64, _i64, ctypes.c_uint, _vp]),
+    "lean_fixed_workspace_bytes": (_i64, []),
     "lean_status_str": (ctypes.c_char_p, [_int]),
 }
 LEAN_MAX_BATCH = 256
@@ -201,6 +203,19 @@ def lean_qmatmul_batch(fmt: int, problems, flags: int = 0, workspace=None,
                                                          ctypes.cast(problems, _vp), flags,
                                                          _addr(workspace), workspace_bytes,
                                                          _stream(stream)))
+
+
+def lean_qmatmul_fixed_ws(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, flags: int = 0,
+                          stream=None) -> None:
+    """M = 1 product whose scratch is the library's own fixed device array (no
+    allocation by the caller; calls overlapping on the GPU must be serialised)."""
+    _check("lean_qmatmul_fixed_ws", _lib.lean_qmatmul_fixed_ws(fmt, _addr(W_packed_dev),
+                                                               _addr(x_dev), _addr(y_dev), N, K,
+                                                               flags, _stream(stream)))
+
+
+def lean_fixed_workspace_bytes() -> int:
+    return _lib.lean_fixed_workspace_bytes()
 
 
 def lean_device_error(clear: bool = True) -> int:

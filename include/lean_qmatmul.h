@@ -191,6 +191,30 @@ lean_status lean_qmatmul_batch(int fmt, int count, const lean_problem *problems,
                                unsigned flags, void *workspace, int64_t workspace_bytes,
                                void *stream);
 
+/* The M = 1 product as lean_qmatmul_ws in workspace (stream-K) mode, with no
+ * allocation by the caller: its scratch is a fixed array inside this library
+ * (lean_fixed_workspace_bytes() bytes, 3 MiB, held on every GPU that loads the
+ * library until the process exits).  The source pages have no counterpart to
+ * this entry point; it serves callers that cannot allocate device memory
+ * where they run the product (code recorded by stream capture, plugins that
+ * must use a host framework's pool, loops that may not risk the
+ * synchronisation of cudaMalloc / cudaFree).
+ *   - Accepts N up to 8388608 rows (262144 row groups); larger N returns
+ *     LEAN_ERR_SHAPE.  W, x, y, flags and stream as for lean_qmatmul_ex.
+ *   - The first call on a device looks up the array's device address (and
+ *     may load the library's kernels); make it before any stream capture.
+ *   - Every call uses the same array: it clears the arrival counters it needs
+ *     (cudaMemsetAsync on `stream`) and overwrites the partial sums, so calls
+ *     that may overlap on the GPU (other streams, other threads) race and
+ *     must be serialised by the caller.  Calls in order on one stream,
+ *     including with LEAN_FLAG_EARLY_WEIGHTS, are safe. */
+lean_status lean_qmatmul_fixed_ws(int fmt, const void *W_packed_dev, const float *x_dev,
+                                  float *y_dev, int64_t N, int64_t K, unsigned flags,
+                                  void *stream);
+
+/* Size in bytes of the fixed array behind lean_qmatmul_fixed_ws. */
+int64_t lean_fixed_workspace_bytes(void);
+
 /* The device error word of the current device: non-zero when a kernel gave up
  * waiting on one of its own pipeline barriers (a bounded wait timed out and
  * the kernel returned early; its outputs are then invalid).  Reads it
