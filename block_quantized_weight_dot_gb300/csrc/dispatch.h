@@ -12,6 +12,10 @@ namespace lean {
 
 constexpr int kMaxBatch = LEAN_MAX_BATCH;  // problems per batched launch
 constexpr int kMaxStreamCtas = 512;        // CTAs of one streaming launch, at most
+#ifndef LEAN_MMA_MIN_M
+#define LEAN_MMA_MIN_M 32
+#endif
+constexpr int64_t kMmaMinM = LEAN_MMA_MIN_M;  // rows of x from which the tensor cores take over
 
 struct HostProb {
     const uint8_t *W;
@@ -39,6 +43,10 @@ lean_status simt_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, 
                      unsigned flags, cudaStream_t stream);
 template <int FMT>
 lean_status dequant_fmt(const Geom &g, const uint8_t *W, float *w, cudaStream_t stream);
+template <int FMT>
+lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
+                    unsigned flags, void *ws, int64_t ws_bytes, unsigned *err,
+                    cudaStream_t stream);
 template <int FMT>
 lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
                        unsigned *err, cudaStream_t stream);

@@ -10,6 +10,7 @@
 #include "../../include/lean_qmatmul.h"
 #include "dispatch.h"
 #include "layout.h"
+#include "qmm_mma.cuh"
 #include "qmm_simt.cuh"
 #include "qmm_stream.cuh"
 
@@ -183,6 +184,100 @@ lean_status dequant_fmt(const Geom &g, const uint8_t *W, float *w, cudaStream_t 
     return cudaGetLastError() == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
 }
 
+// --------------------------------------------------------- tensor-core path ---
+
+// K split of the tensor-core product: the cluster size that minimises
+// waves x (K blocks per CTA + a fixed cost of about four blocks for set-up
+// and epilogue), never more K blocks' worth of CTAs than there are blocks.
+inline int mma_split(int64_t tiles, int nkb, int64_t slots) {
+    int ks = 1;
+    double best = 1e300;
+    for (int c = 1; c <= kMmaMaxSplit && c <= nkb; ++c) {
+        const int64_t waves = (tiles * c + slots - 1) / slots;
+        const double cost = (double)waves * ((nkb + c - 1) / c + 4.0);
+        if (cost < best - 1e-9) {
+            best = cost;
+            ks = c;
+        }
+    }
+    return ks;
+}
+
+template <int FMT>
+lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
+                    unsigned flags, void *ws, int64_t ws_bytes, unsigned *err,
+                    cudaStream_t stream) {
+    static std::atomic<uint64_t> smem_done{0}, smem_done_x{0};
+    const int64_t tiles = (g.N + kMmaRows - 1) / kMmaRows;
+    const int nkb = (int)((g.K + kMmaKB - 1) / kMmaKB);
+    const int64_t mtiles = (M + kMmaMaxN - 1) / kMmaMaxN;
+    const int mpad = ((int)std::min<int64_t>(M, kMmaMaxN) + 15) & ~15;
+    const int S = mma_stages<FMT>(mpad);
+    const size_t smem = 1024 + (size_t)S * mma_stage_bytes<FMT>(mpad);
+    // one CTA per SM (the ring takes most of the shared memory)
+    const int ks = mma_split(tiles * mtiles, nkb, (int64_t)sm_count());
+    if (tiles * ks > INT32_MAX) return LEAN_ERR_SHAPE;
+    const int64_t xs_bytes = mma_xs_bytes(M, g.K);
+    if (ws && ws_bytes < xs_bytes) return LEAN_ERR_SHAPE;
+    uint8_t *xs = static_cast<uint8_t *>(ws);
+    MmaArgs a = {};
+    a.W = W;
+    a.x = x;
+    a.xs = xs;
+    a.y = y;
+    a.N = (int)g.N;
+    a.K = (int)g.K;
+    a.M = (int)M;
+    a.ks = ks;
+    a.nkb = nkb;
+    a.S = S;
+    a.groups = g.groups;
+    a.steps = g.steps;
+    a.last_blocks = g.last_blocks;
+    a.step_vecs = g.step_vecs;
+    a.group_vecs = g.group_vecs;
+    a.err = err;
+    a.mg = make_magic();
+    if (xs) {
+        // x -> bf16 hi / lo operand tiles, once
+        XsplitArgs xa;
+        xa.x = x;
+        xa.xs = xs;
+        xa.M = (int)M;
+        xa.K = (int)g.K;
+        xa.nkb = nkb;
+        xa.mtiles = (int)mtiles;
+        xa.rows = (mtiles - 1) * kMmaMaxN + (((M - (mtiles - 1) * kMmaMaxN) + 15) & ~15);
+        const int64_t blocks = (xa.rows * nkb * 8 + 255) / 256;
+        if (blocks > INT32_MAX) return LEAN_ERR_SHAPE;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        fill_launch(cfg, attr, 1, flags);
+        if (cudaLaunchKernelEx(&cfg, xsplit_kernel, xa) != cudaSuccess) return LEAN_ERR_CUDA;
+    }
+    auto kern = xs ? qmm_mma_kernel<FMT, true> : qmm_mma_kernel<FMT, false>;
+    std::atomic<uint64_t> &sd = xs ? smem_done : smem_done_x;
+    if (!ensure_smem(kern, (size_t)kMmaSmemLimit, sd)) return LEAN_ERR_CUDA;
+    for (int64_t t0 = 0; t0 < mtiles; t0 += 65535) {
+        a.m_base = (int)(t0 * kMmaMaxN);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim =
+            dim3((unsigned)(tiles * ks), (unsigned)std::min<int64_t>(65535, mtiles - t0), 1);
+        cfg.blockDim = dim3(kMmaThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        // after the split kernel (which itself starts only when the caller's
+        // flags allow) the launch is always programmatic
+        fill_launch(cfg, attr, ks, xs ? (unsigned)LEAN_FLAG_EARLY_WEIGHTS : flags);
+        if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return LEAN_ERR_CUDA;
+    }
+    return LEAN_OK;
+}
+
 // -------------------------------------------------------------- stream path ---
 
 // Total row groups of a problem list; false when the list is too long.
@@ -273,4 +368,7 @@ lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int6
                                        int64_t, unsigned, cudaStream_t);                       \
     template lean_status dequant_fmt<FMT>(const Geom &, const uint8_t *, float *, cudaStream_t); \
     template lean_status stream_fmt<FMT>(const HostProb *, int, unsigned, void *, int64_t,     \
-                                         unsigned *, cudaStream_t);
+                                         unsigned *, cudaStream_t);                            \
+    template lean_status mma_fmt<FMT>(const Geom &, const uint8_t *, const float *, float *,   \
+                                      int64_t, unsigned, void *, int64_t, unsigned *,          \
+                                      cudaStream_t);

@@ -9,6 +9,7 @@
 #include "../../include/lean_qmatmul.h"
 #include "dispatch.h"
 #include "layout.h"
+#include "qmm_mma.cuh"
 
 using namespace lean;
 
@@ -82,6 +83,19 @@ lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_de
         HostProb hp = {W, x_dev, y_dev, g};
         return dispatch_stream(fmt, &hp, 1, flags, workspace, workspace_bytes, s);
     }
+    if (M >= kMmaMinM) {
+        unsigned *err = error_word();
+        if (!err) return LEAN_ERR_CUDA;
+        void *ws = workspace;
+        const int64_t wsb = workspace_bytes;
+        switch (fmt) {
+        case LEAN_Q4_0: return mma_fmt<Q4_0>(g, W, x_dev, y_dev, M, flags, ws, wsb, err, s);
+        case LEAN_Q8_0: return mma_fmt<Q8_0>(g, W, x_dev, y_dev, M, flags, ws, wsb, err, s);
+        case LEAN_I8_B64: return mma_fmt<I8_B64>(g, W, x_dev, y_dev, M, flags, ws, wsb, err, s);
+        case LEAN_Q6_K: return mma_fmt<Q6_K>(g, W, x_dev, y_dev, M, flags, ws, wsb, err, s);
+        }
+        return LEAN_ERR_FORMAT;
+    }
     switch (fmt) {
     case LEAN_Q4_0: return simt_fmt<Q4_0>(g, W, x_dev, y_dev, M, flags, s);
     case LEAN_Q8_0: return simt_fmt<Q8_0>(g, W, x_dev, y_dev, M, flags, s);
@@ -104,6 +118,7 @@ lean_status lean_qmatmul(int fmt, const void *W_packed_dev, const float *x_dev, 
 int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M) {
     Geom g;
     if (M <= 0 || !make_geom(fmt, N, K, &g)) return -1;
+    if (M >= kMmaMinM) return mma_xs_bytes(M, K);
     if (M > 1) return 0;
     return workspace_layout(g.groups).total;
 }

@@ -15,15 +15,21 @@ def torch_cuda():
     return torch
 
 
-def run_gpu(fmt, W_canon, x, N, K, stream=None):
-    """Pack on the host, upload, call lean_qmatmul, return y as float64 numpy."""
+def run_gpu(fmt, W_canon, x, N, K, stream=None, workspace=False):
+    """Pack on the host, upload, call lean_qmatmul (or lean_qmatmul_ws with a
+    workspace of the queried size), return y as float64 numpy."""
     torch = torch_cuda()
     from block_quantized_weight_dot_gb300 import lean
     Wd = lean.upload_packed(fmt, W_canon, N, K)
     xd = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32).reshape(-1, K)).cuda()
     M = xd.shape[0]
     yd = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-    lean.lean_qmatmul(fmt, Wd, xd, yd, N, K, M, stream)
+    if workspace:
+        nb = lean.lean_qmatmul_workspace_bytes(fmt, N, K, M)
+        ws = torch.zeros((max(nb, 256),), dtype=torch.uint8, device="cuda")
+        lean.lean_qmatmul_ws(fmt, Wd, xd, yd, N, K, M, 0, ws, nb, stream)
+    else:
+        lean.lean_qmatmul(fmt, Wd, xd, yd, N, K, M, stream)
     torch.cuda.synchronize()
     return yd.cpu().numpy().astype(np.float64)
 

@@ -56,6 +56,19 @@ def test_sizes(lean):
     assert lean.lean_packed_bytes(0, 960, 960) == 30 * 30 * 512 + 30 * 4 * 512
 
 
+def test_workspace_sizes(lean):
+    """M = 1: stream-K scratch; 2..31 rows: none; 32 rows and up: x split
+    into bf16 hi + lo (4 bytes per element) over rows padded to 16 within each
+    256-row tile and K padded to 64."""
+    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 1) > 0
+    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 31) == 0
+    assert lean.lean_qmatmul_workspace_bytes(0, 2048, 2048, 256) == 256 * 2048 * 4
+    assert lean.lean_qmatmul_workspace_bytes(0, 2048, 2048, 32) == 32 * 2048 * 4
+    assert lean.lean_qmatmul_workspace_bytes(0, 100, 96, 33) == 48 * 128 * 4
+    assert lean.lean_qmatmul_workspace_bytes(0, 100, 96, 257) == (256 + 16) * 128 * 4
+    assert lean.lean_qmatmul_workspace_bytes(0, 100, 96, 0) == -1
+
+
 @pytest.mark.parametrize("fmt", range(4), ids=[syn.FORMAT_NAMES[f] for f in range(4)])
 def test_pack_round_trip(lean, fmt):
     be = syn.BLOCK_ELEMS[fmt]
