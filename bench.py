@@ -213,12 +213,18 @@ class DeviceWorkload:
             self.launches_per_step = 1
             return
         n = 0
+        tc_min = lean.lean_tensor_core_min_m()
         for i, lin in enumerate(self.lins):
             x = self.x.data_ptr() + 4 * self.x_off[i]
             y = self.y.data_ptr() + 4 * self.y_off[i]
             lean.lean_qmatmul_ws(lin.fmt, self.W[copy][i], x, y, lin.N, lin.K, lin.M,
                                  self.flags, self.ws, self.ws_bytes, stream)
-            n += 1 if lin.M == 1 else (lin.M + 15) // 16
+            if lin.M == 1:
+                n += 1
+            elif lin.M < tc_min:
+                n += (lin.M + 15) // 16       # CUDA-core kernel per 16 rows of x
+            else:
+                n += 2                        # x split + tensor-core product
         self.launches_per_step = n
 
     def capture(self, stream):

@@ -13,7 +13,7 @@ namespace lean {
 constexpr int kMaxBatch = LEAN_MAX_BATCH;  // problems per batched launch
 constexpr int kMaxStreamCtas = 512;        // CTAs of one streaming launch, at most
 #ifndef LEAN_MMA_MIN_M
-#define LEAN_MMA_MIN_M 32
+#define LEAN_MMA_MIN_M 16
 #endif
 constexpr int64_t kMmaMinM = LEAN_MMA_MIN_M;  // rows of x from which the tensor cores take over
 

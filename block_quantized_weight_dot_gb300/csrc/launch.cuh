@@ -187,14 +187,14 @@ lean_status dequant_fmt(const Geom &g, const uint8_t *W, float *w, cudaStream_t 
 // --------------------------------------------------------- tensor-core path ---
 
 // K split of the tensor-core product: the cluster size that minimises
-// waves x (K blocks per CTA + a fixed cost of about four blocks for set-up
-// and epilogue), never more K blocks' worth of CTAs than there are blocks.
-inline int mma_split(int64_t tiles, int nkb, int64_t slots) {
+// waves x (256-wide K slots per CTA + a fixed cost of about one slot for
+// set-up and epilogue), never more CTAs than slots.
+inline int mma_split(int64_t tiles, int nsl, int64_t slots) {
     int ks = 1;
     double best = 1e300;
-    for (int c = 1; c <= kMmaMaxSplit && c <= nkb; ++c) {
+    for (int c = 1; c <= kMmaMaxSplit && c <= nsl; ++c) {
         const int64_t waves = (tiles * c + slots - 1) / slots;
-        const double cost = (double)waves * ((nkb + c - 1) / c + 4.0);
+        const double cost = (double)waves * ((nsl + c - 1) / c + 1.0);
         if (cost < best - 1e-9) {
             best = cost;
             ks = c;
@@ -210,13 +210,15 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
     static std::atomic<uint64_t> smem_done{0}, smem_done_x{0};
     const int64_t tiles = (g.N + kMmaRows - 1) / kMmaRows;
     const int nkb = (int)((g.K + kMmaKB - 1) / kMmaKB);
+    const int nsl = (nkb + kMmaSub - 1) / kMmaSub;
     const int64_t mtiles = (M + kMmaMaxN - 1) / kMmaMaxN;
     const int mpad = ((int)std::min<int64_t>(M, kMmaMaxN) + 15) & ~15;
-    const int S = mma_stages<FMT>(mpad);
-    const size_t smem = 1024 + (size_t)S * mma_stage_bytes<FMT>(mpad);
-    // one CTA per SM (the ring takes most of the shared memory)
-    const int ks = mma_split(tiles * mtiles, nkb, (int64_t)sm_count());
-    if (tiles * ks > INT32_MAX) return LEAN_ERR_SHAPE;
+    const int RS = mma_raw_slots<FMT>(mpad);
+    const size_t smem = (size_t)mma_smem_bytes<FMT>(mpad, RS);
+    // one CTA per SM: the rings take most of the shared memory and all 512
+    // tensor-memory columns are allocated
+    const int ks = mma_split(tiles * mtiles, nsl, (int64_t)sm_count());
+    if (tiles * ks > INT32_MAX || RS < 1) return LEAN_ERR_SHAPE;
     const int64_t xs_bytes = mma_xs_bytes(M, g.K);
     if (ws && ws_bytes < xs_bytes) return LEAN_ERR_SHAPE;
     uint8_t *xs = static_cast<uint8_t *>(ws);
@@ -230,7 +232,10 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
     a.M = (int)M;
     a.ks = ks;
     a.nkb = nkb;
-    a.S = S;
+    a.nsl = nsl;
+    a.RS = RS;
+    a.BS = mma_b_stages(mpad);
+    a.raw_off = mma_raw_off(mpad);
     a.groups = g.groups;
     a.steps = g.steps;
     a.last_blocks = g.last_blocks;

@@ -115,6 +115,8 @@ lean_status lean_qmatmul(int fmt, const void *W_packed_dev, const float *x_dev, 
     return lean_qmatmul_ws(fmt, W_packed_dev, x_dev, y_dev, N, K, M, 0u, nullptr, 0, stream);
 }
 
+int lean_tensor_core_min_m(void) { return (int)kMmaMinM; }
+
 int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M) {
     Geom g;
     if (M <= 0 || !make_geom(fmt, N, K, &g)) return -1;

@@ -2,36 +2,49 @@
 // (tcgen05.mma with accumulators in tensor memory).
 //
 // With many rows of x the product is a dense contraction.  The pages' GPU
-// path dequantizes weight tiles in shared memory and multiplies them there
-// ("oxinfer" crate page, Platforms and accelerators: Browser (WebGPU)), in
-// f32.  bf16 operands alone would miss the 1e-4 tolerance (one bf16 rounding
-// is 2^-9 relative), so each operand is split into a bf16 pair, w = w_hi +
-// w_lo and x = x_hi + x_lo, and three MMAs accumulate w_hi*x_hi + w_hi*x_lo +
-// w_lo*x_hi in fp32.  The dropped w_lo*x_lo and the rounding of x_lo (and of
-// w_lo for the formats whose dequantized weights need more than 16 bits) are
-// each below 2^-16 of |w*x|; for Q4_0 the weight split is exact, since
-// d*(q-8) has at most 15 significant bits.
+// path dequantizes weight tiles and multiplies them in f32 ("oxinfer" crate
+// page, Platforms and accelerators: Browser (WebGPU)).  bf16 operands alone
+// would miss the 1e-4 tolerance (one bf16 rounding is 2^-9 relative), so each
+// operand is split into a bf16 pair, w = w_hi + w_lo and x = x_hi + x_lo, and
+// three MMAs accumulate w_hi*x_hi + w_hi*x_lo + w_lo*x_hi in fp32.  The
+// dropped w_lo*x_lo and the rounding of x_lo (and of w_lo for the formats
+// whose dequantized weights need more than 16 bits) are each below 2^-16 of
+// |w*x|; for Q4_0 the weight split is exact, since d*(q-8) has at most 15
+// significant bits.
 //
 // Two kernels.  xsplit_kernel writes x once as bf16 hi / lo tiles already in
 // the shared-memory operand layout, one contiguous piece per (256-row tile of
 // x, 64-wide K block), into a caller workspace; without one, the converter
-// warps split each CTA's x themselves.  qmm_mma_kernel then computes D = W_tile * X^T for 128
-// weight rows against up to 256 rows of x -- one tcgen05.mma of shape M=128
-// (weight rows) x N=mpad (rows of x padded to 16) x K=16, D (= y^T) in tensor
-// memory -- with three roles over an S-stage shared-memory ring:
-//   warp 8 (one lane)   TMA bulk copies of the stage's packed weight vectors
-//                       and of its x operand piece (complete_tx on full[s]);
-//   warps 0-7           dequantize and split the weights of the stage (thread
-//                       t: row t%128, half t/128 of the 64-wide block) into
-//                       the A operand, then arrive on conv[s];
-//   warp 9 (one lane)   issues the stage's 12 MMAs once conv[s] completes and
-//                       commits them to empty[s], which frees the stage.
+// warps split each CTA's x themselves.  qmm_mma_kernel computes
+// D = W_tile * X^T for 128 weight rows against up to 256 rows of x: one
+// tcgen05.mma of shape M=128 (weight rows) x N=mpad (rows of x padded to 16)
+// x K=16, with A (the split weights) and D (= y^T) in tensor memory and B
+// (the split x) in shared memory.  Roles:
+//   warp 8 (one lane)   streams the packed weights with one TMA bulk copy per
+//                       32-row group and 256-wide K slot into a deep ring of
+//                       raw slots (raw_full / raw_empty);
+//   warp 10 (one lane)  with split x, copies each 64-wide K block of it into a
+//                       ring of B stages (b_full);
+//   warps 0-7           per 64-wide K block, dequantize and split the weights
+//                       (thread t: row t%128, half t/128 of the block) and
+//                       write them to a tensor-memory A stage with tcgen05.st
+//                       (a_full); without split x they also fill B;
+//   warps 9, 11-13      (one lane each) issue the block's 12 MMAs and commit
+//                       them to the A stage's barrier mma_done, which frees
+//                       both the A stage and the block's B stage (the B ring
+//                       is no deeper than the A ring, so a B stage's last
+//                       user is found on the A ring).  A warp can issue one
+//                       MMA every ~55 cycles whatever N is, while the tensor
+//                       core needs 128 * N / 256 cycles for one, so for small
+//                       N up to four warps share the 16-wide K steps, each
+//                       accumulating into its own columns of tensor memory;
+//                       the epilogue adds the accumulators in a fixed order.
 // When the row tiles alone do not fill the GPU, a thread-block cluster of ks
-// CTAs splits K; each CTA leaves its partial D in shared memory and, after a
-// cluster barrier, CTA r sums columns r*mpad/ks .. (r+1)*mpad/ks of all ks
-// partials in rank order through distributed shared memory (deterministic,
-// no atomics).  Tiles of x beyond the first 256 rows are gridDim.y.  Every
-// wait is bounded; a timeout sets the device error word.
+// CTAs splits K on slot boundaries; each CTA leaves its partial D in shared
+// memory and, after a cluster barrier, CTA r sums columns r*mpad/ks ..
+// (r+1)*mpad/ks of all ks partials in rank order through distributed shared
+// memory (deterministic, no atomics).  Tiles of x beyond the first 256 rows
+// are gridDim.y.  Every wait is bounded; a timeout sets the device error word.
 #pragma once
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -44,49 +57,64 @@
 
 namespace lean {
 
-constexpr int kMmaRows = 128;       // weight rows per tile (MMA M)
-constexpr int kMmaKB = 64;          // K per pipeline stage
-constexpr int kMmaConvThreads = 256;  // warps 0-7
-constexpr int kMmaThreads = 320;    // + producer warp 8 + MMA warp 9
-constexpr int kMmaMaxN = 256;       // rows of x per tile (MMA N)
-constexpr int kMmaMaxSplit = 8;     // CTAs of a K-splitting cluster
-constexpr int kMmaMaxStages = 4;
+constexpr int kMmaRows = 128;          // weight rows per tile (MMA M)
+constexpr int kMmaKB = 64;             // K per MMA stage
+constexpr int kMmaSlotK = 256;         // K per raw weight slot
+constexpr int kMmaSub = kMmaSlotK / kMmaKB;  // MMA stages per raw slot
+constexpr int kMmaConvThreads = 256;   // warps 0-7
+constexpr int kMmaThreads = 448;       // + weight producer 8, x producer 10, MMA 9, 11-13
+constexpr int kMmaMaxIssuers = 4;      // warps issuing MMAs, each into its own accumulator
+constexpr int kMmaMaxN = 256;          // rows of x per tile (MMA N)
+constexpr int kMmaMaxSplit = 8;        // CTAs of a K-splitting cluster
+constexpr int kMmaMaxRaw = 8;          // raw weight slots, at most
+constexpr int kMmaMaxB = 4;            // B stages, at most (no more than A stages)
+constexpr int kMmaBBudget = 32 * 1024;   // shared memory for the B ring, about
+constexpr int kMmaAStages = 4;         // tensor-memory A stages
 constexpr int kMmaSmemLimit = 227 * 1024;
+constexpr uint32_t kMmaTmemCols = 512;  // D: columns 0..255, A stages: 256..511
+constexpr uint32_t kMmaDCols = 256;
+constexpr uint32_t kMmaACols = 64;      // one A stage: hi in 32 columns, lo in 32
 constexpr uint64_t kMmaWaitNs = 2000000000ull;
 
 constexpr unsigned kErrMmaTimeout = 4u;
 
-// Packed vectors copied per 32-row group and stage: QV quant vectors, XV
-// extra vectors (Q6_K sub-scales), then the step's scale vector.
+// Raw slot of one 32-row group: QV packed vectors of the slot's 256-wide K
+// range (Q6_K: the 13 of one super-block), then the step's scale vector.
 template <int FMT> struct MmaRaw;
-template <> struct MmaRaw<Q4_0> { static constexpr int QV = 2, XV = 0; };
-template <> struct MmaRaw<Q8_0> { static constexpr int QV = 4, XV = 0; };
-template <> struct MmaRaw<I8_B64> { static constexpr int QV = 4, XV = 0; };
-template <> struct MmaRaw<Q6_K> { static constexpr int QV = 3, XV = 1; };
+template <> struct MmaRaw<Q4_0> { static constexpr int QV = 8; };
+template <> struct MmaRaw<Q8_0> { static constexpr int QV = 16; };
+template <> struct MmaRaw<I8_B64> { static constexpr int QV = 16; };
+template <> struct MmaRaw<Q6_K> { static constexpr int QV = 13; };
 template <int FMT>
 __host__ __device__ constexpr int mma_raw_group_bytes() {
-    return (MmaRaw<FMT>::QV + MmaRaw<FMT>::XV + 1) * kVecBytes;
+    return (MmaRaw<FMT>::QV + 1) * kVecBytes;
 }
 template <int FMT>
 __host__ __device__ constexpr int mma_raw_bytes() {
     return (kMmaRows / kRowsPerGroup) * mma_raw_group_bytes<FMT>();
 }
 
-// One stage: raw weight vectors, A_hi, A_lo (128 x 64 bf16), B_hi, B_lo
-// (mpad x 64 bf16).  Shared memory = 1 KiB of barriers + S stages.
-__host__ __device__ constexpr int mma_a_bytes() { return kMmaRows * kMmaKB * 2; }
+// B stage: B_hi, B_lo (mpad x 64 bf16 each) in the layout of tile_off.
 __host__ __device__ inline int mma_b_bytes(int mpad) { return mpad * kMmaKB * 2; }
-template <int FMT>
-__host__ __device__ inline int mma_stage_bytes(int mpad) {
-    return mma_raw_bytes<FMT>() + 2 * mma_a_bytes() + 2 * mma_b_bytes(mpad);
+// B stages: as many as fit the budget (x comes from L2, and a stage is
+// refilled only once its MMAs are done), at least two (the K-split partials
+// reuse the ring: 2 stages hold 128 x mpad fp32), at most the A stages.
+__host__ __device__ inline int mma_b_stages(int mpad) {
+    const int s = kMmaBBudget / (2 * mma_b_bytes(mpad));
+    return s < 2 ? 2 : s > kMmaMaxB ? kMmaMaxB : s;
+}
+// Shared memory: 1 KiB of barriers, the B ring, then the raw ring.
+__host__ __device__ inline int mma_raw_off(int mpad) {
+    return 1024 + mma_b_stages(mpad) * 2 * mma_b_bytes(mpad);
 }
 template <int FMT>
-__host__ __device__ inline int mma_stages(int mpad) {
-    const int s = (kMmaSmemLimit - 1024) / mma_stage_bytes<FMT>(mpad);
-    return s < kMmaMaxStages ? s : kMmaMaxStages;
+__host__ __device__ inline int mma_raw_slots(int mpad) {
+    const int s = (kMmaSmemLimit - mma_raw_off(mpad)) / mma_raw_bytes<FMT>();
+    return s < kMmaMaxRaw ? s : kMmaMaxRaw;
 }
-__host__ __device__ inline uint32_t mma_tmem_cols(int mpad) {
-    return mpad <= 32 ? 32u : mpad <= 64 ? 64u : mpad <= 128 ? 128u : 256u;
+template <int FMT>
+__host__ __device__ inline int mma_smem_bytes(int mpad, int raw_slots) {
+    return mma_raw_off(mpad) + raw_slots * mma_raw_bytes<FMT>();
 }
 
 // Split x: for each 256-row tile t of x (mpad_t rows, padded to 16) and each
@@ -103,18 +131,20 @@ inline int64_t mma_xs_bytes(int64_t M, int64_t K) {
 }
 
 struct MmaArgs {
-    const uint8_t *W;  // packed weights
-    const float *x;    // x[M][K]
-    const uint8_t *xs; // split x, or null
-    float *y;          // y[M][N]
+    const uint8_t *W;   // packed weights
+    const float *x;     // x[M][K]
+    const uint8_t *xs;  // split x, or null
+    float *y;           // y[M][N]
     int N, K, M;
-    int ks;            // CTAs splitting K (cluster size)
-    int nkb;           // 64-wide K blocks
-    int m_base;        // first row of x of this launch
-    int S;             // pipeline stages
-    int pad;
+    int ks;             // CTAs splitting K (cluster size)
+    int nkb;            // 64-wide K blocks
+    int nsl;            // 256-wide K slots
+    int m_base;         // first row of x of this launch
+    int RS;             // raw weight slots
+    int BS;             // B stages
+    int raw_off;        // byte offset of the raw ring in shared memory
+    int steps, last_blocks, step_vecs;
     int64_t groups;
-    int steps, last_blocks, step_vecs, pad2;
     int64_t group_vecs;
     unsigned *err;
     Magic mg;
@@ -149,13 +179,13 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T: bf16 operands, fp32 accumulators
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T: bf16 operands, fp32 accumulators
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // arrive on `bar` once every MMA issued so far by this thread has completed
@@ -178,6 +208,36 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// 16 consecutive 32-bit columns of one tensor-memory lane per thread
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// sum over the n accumulators (stride `cols` columns) of 32 fp32 columns,
+// in accumulator order; zeros when !have
+__device__ __forceinline__ void tmem_sum32(uint32_t taddr, int n, uint32_t cols, bool have,
+                                           uint32_t (&r)[32]) {
+    if (!have) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+        return;
+    }
+    tmem_ld32(taddr, r);
+    for (int k = 1; k < n; ++k) {
+        uint32_t t[32];
+        tmem_ld32(taddr + k * cols, t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(t[i]));
+    }
 }
 
 // Shared-memory matrix descriptor, K-major, no swizzle: core matrices of
@@ -202,17 +262,20 @@ __host__ __device__ __forceinline__ uint32_t tile_off(int rows, int r, int k) {
                       (r & 7) * 16 + (k & 7) * 2);
 }
 
+// bf16 hi / lo halves of two fp32 values, packed low element first
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 bh = __floats2bfloat162_rn(a, b);
+    const float2 fh = __bfloat1622float2(bh);
+    const __nv_bfloat162 bl = __floats2bfloat162_rn(a - fh.x, b - fh.y);
+    hi = *reinterpret_cast<const uint32_t *>(&bh);
+    lo = *reinterpret_cast<const uint32_t *>(&bl);
+}
+
 // split 8 fp32 values into bf16 hi / lo halves and store 16 bytes of each
 __device__ __forceinline__ void split_store8(const float *v, uint8_t *hi, uint8_t *lo) {
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 bh = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-        const float2 fh = __bfloat1622float2(bh);
-        const __nv_bfloat162 bl = __floats2bfloat162_rn(v[2 * i] - fh.x, v[2 * i + 1] - fh.y);
-        h[i] = *reinterpret_cast<const uint32_t *>(&bh);
-        l[i] = *reinterpret_cast<const uint32_t *>(&bl);
-    }
+    for (int i = 0; i < 4; ++i) split2(v[2 * i], v[2 * i + 1], h[i], l[i]);
     *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
@@ -249,17 +312,58 @@ static __global__ void __launch_bounds__(256) xsplit_kernel(const XsplitArgs a) 
     split_store8(v, piece + off, piece + mma_b_bytes(mpad) + off);
 }
 
-// ---- weights: raw vectors in shared memory -> exact fp32 ------------------------------
-// 32 elements 32*half .. 32*half+31 of the stage's 64-wide K block for one
-// row; rv points at the row's 16 bytes of its group's first raw vector.
+// ---- weights: packed vectors -> raw slot ------------------------------------------
+// Bytes of global slot gs (K range 256*gs .. 256*gs+255) of one row group,
+// and, when bar is given, the TMA copies that bring them into dst: the
+// slot's quant vectors at 0, the step's scale vector at QV.
 template <int FMT>
-__device__ __forceinline__ void raw_chunk32(const uint8_t *rv, int half, int sidx, int64_t kb,
+__device__ __forceinline__ uint32_t raw_copy(const MmaArgs &a, int64_t gi, int64_t gs,
+                                             uint8_t *dst, uint64_t *bar) {
+    constexpr int VPB = BlockTraits<FMT>::VPB, QV = MmaRaw<FMT>::QV;
+    // step holding the slot and the slot's first block in it
+    int64_t s;
+    int i0;
+    if (FMT == Q4_0 || FMT == Q8_0) {
+        s = gs;
+        i0 = 0;
+    } else if (FMT == I8_B64) {
+        s = gs >> 1;
+        i0 = 4 * (int)(gs & 1);
+    } else {
+        s = gs >> 3;
+        i0 = (int)(gs & 7);
+    }
+    const int nblk = s == a.steps - 1 ? a.last_blocks : 8;
+    const int nb = FMT == Q4_0 || FMT == Q8_0 ? nblk : FMT == I8_B64 ? min(4, nblk - i0) : 1;
+    const uint32_t qbytes = (uint32_t)(nb * VPB * kVecBytes);
+    if (bar) {
+        const uint8_t *step = a.W + (gi * a.group_vecs + s * a.step_vecs) * kVecBytes;
+        if ((FMT == Q4_0 || FMT == Q8_0) && nb == 8) {
+            // a whole step: quant vectors and the scale vector are contiguous
+            bulk_g2s(dst, step, qbytes + kVecBytes, bar);
+        } else {
+            bulk_g2s(dst, step + i0 * VPB * kVecBytes, qbytes, bar);
+            bulk_g2s(dst + QV * kVecBytes, step + nblk * VPB * kVecBytes, kVecBytes, bar);
+        }
+    }
+    return qbytes + kVecBytes;
+}
+
+// Dequantized weights of one row: 32 elements 32*half .. 32*half+31 of the
+// 64-wide K block kb; rv points at the row's 16 bytes of its group's raw slot.
+template <int FMT>
+__device__ __forceinline__ void raw_chunk32(const uint8_t *rv, int half, int64_t kb,
                                             const Magic &mg, float (&w)[32]) {
-    constexpr int QV = MmaRaw<FMT>::QV, XV = MmaRaw<FMT>::XV;
-    const float d = h2f(reinterpret_cast<const unsigned short *>(rv + (QV + XV) * kVecBytes)[sidx]);
+    constexpr int QV = MmaRaw<FMT>::QV;
+    const int sub = (int)(kb & (kMmaSub - 1));
+    // scale slot of the block in its step's scale vector
+    const int sidx = FMT == Q4_0 || FMT == Q8_0 ? 2 * sub + half
+                     : FMT == I8_B64           ? (int)(kb & 7)
+                                               : (int)((kb >> 2) & 7);
+    const float d = h2f(reinterpret_cast<const unsigned short *>(rv + QV * kVecBytes)[sidx]);
     const f32x2 dd = pack2(d, d);
-    if (FMT == Q4_0) {  // vector h = block 2kb + h
-        const uint4 v = *reinterpret_cast<const uint4 *>(rv + half * kVecBytes);
+    if (FMT == Q4_0) {  // block 2*sub + half of the step is vector 2*sub + half
+        const uint4 v = *reinterpret_cast<const uint4 *>(rv + (2 * sub + half) * kVecBytes);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             f32x2 p[4];
@@ -271,10 +375,13 @@ __device__ __forceinline__ void raw_chunk32(const uint8_t *rv, int half, int sid
                 w[8 * t + 2 * j + 1] = q.y;
             }
         }
-    } else if (FMT == Q8_0 || FMT == I8_B64) {  // vectors 2h, 2h+1: 16 elements each
+    } else if (FMT == Q8_0 || FMT == I8_B64) {
+        // Q8_0: block 2*sub + half, its vectors 0, 1; I8_B64: block sub, its
+        // vectors 2*half, 2*half + 1 (vector j holds elements 16j .. 16j+15)
+        const int v0 = FMT == Q8_0 ? 2 * (2 * sub + half) : 4 * sub + 2 * half;
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(rv + (2 * half + jj) * kVecBytes);
+            const uint4 v = *reinterpret_cast<const uint4 *>(rv + (v0 + jj) * kVecBytes);
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 f32x2 p[2];
@@ -287,18 +394,17 @@ __device__ __forceinline__ void raw_chunk32(const uint8_t *rv, int half, int sid
                 }
             }
         }
-    } else {  // Q6_K: vectors 0..2 hold sub-blocks 4p..4p+3 (p = kb % 4); this half 2 of them
-        const int p = (int)(kb & 3);
-        const uint4 va = *reinterpret_cast<const uint4 *>(rv + half * kVecBytes);
-        const uint4 vb = *reinterpret_cast<const uint4 *>(rv + (half + 1) * kVecBytes);
-        const uint4 vs = *reinterpret_cast<const uint4 *>(rv + QV * kVecBytes);
+    } else {  // Q6_K: sub-blocks 4*sub + 2*half, +1 sit in words 12*sub + 6*half .. +5
+        const uint4 va = *reinterpret_cast<const uint4 *>(rv + (3 * sub + half) * kVecBytes);
+        const uint4 vb = *reinterpret_cast<const uint4 *>(rv + (3 * sub + half + 1) * kVecBytes);
+        const uint4 vs = *reinterpret_cast<const uint4 *>(rv + 12 * kVecBytes);
         uint32_t wd[6];
         if (half == 0) {
             wd[0] = va.x; wd[1] = va.y; wd[2] = va.z; wd[3] = va.w; wd[4] = vb.x; wd[5] = vb.y;
         } else {
             wd[0] = va.z; wd[1] = va.w; wd[2] = vb.x; wd[3] = vb.y; wd[4] = vb.z; wd[5] = vb.w;
         }
-        const uint32_t scw = word_of(vs, p);
+        const uint32_t scw = word_of(vs, sub);
 #pragma unroll
         for (int sb = 0; sb < 2; ++sb) {
             f32x2 q6[8];
@@ -315,146 +421,143 @@ __device__ __forceinline__ void raw_chunk32(const uint8_t *rv, int half, int sid
     }
 }
 
-// Weight copies of stage kb for group gi into the raw slot of that group;
-// returns the bytes they bring (0 for a group past the last one).
-template <int FMT>
-__device__ __forceinline__ uint32_t raw_bytes_of(const MmaArgs &a, int64_t gi, int64_t kb) {
-    constexpr int VPB = BlockTraits<FMT>::VPB;
-    if (gi >= a.groups) return 0;
-    if (FMT == Q4_0 || FMT == Q8_0) {
-        const int nb = (2 * kb + 1 < (int64_t)a.K / 32) ? 2 : 1;
-        return (uint32_t)((nb * VPB + 1) * kVecBytes);
-    }
-    return (uint32_t)((MmaRaw<FMT>::QV + MmaRaw<FMT>::XV + 1) * kVecBytes);
-}
-template <int FMT>
-__device__ __forceinline__ void raw_copy(const MmaArgs &a, int64_t gi, int64_t kb, uint8_t *dst,
-                                         uint64_t *bar) {
-    constexpr int VPB = BlockTraits<FMT>::VPB, QV = MmaRaw<FMT>::QV, XV = MmaRaw<FMT>::XV;
-    const int64_t c = FMT == Q6_K ? (kb >> 2) : FMT == I8_B64 ? kb : 2 * kb;  // first block
-    const int s = (int)(c >> 3), i = (int)(c & 7);
-    const int nblk = s == a.steps - 1 ? a.last_blocks : 8;
-    const uint8_t *step = a.W + (gi * a.group_vecs + (int64_t)s * a.step_vecs) * kVecBytes;
-    if (FMT == Q4_0 || FMT == Q8_0) {
-        const int nb = (2 * kb + 1 < (int64_t)a.K / 32) ? 2 : 1;
-        bulk_g2s(dst, step + i * VPB * kVecBytes, nb * VPB * kVecBytes, bar);
-    } else if (FMT == I8_B64) {
-        bulk_g2s(dst, step + i * VPB * kVecBytes, VPB * kVecBytes, bar);
-    } else {
-        const int p = (int)(kb & 3);
-        bulk_g2s(dst, step + (i * VPB + 3 * p) * kVecBytes, 3 * kVecBytes, bar);
-        bulk_g2s(dst + QV * kVecBytes, step + (i * VPB + 12) * kVecBytes, kVecBytes, bar);
-    }
-    bulk_g2s(dst + (QV + XV) * kVecBytes, step + nblk * VPB * kVecBytes, kVecBytes, bar);
-}
-
 // ---- the product ----------------------------------------------------------------------
-// grid = (ceil(N/128) * ks, tiles of x); cluster = (ks, 1, 1); 320 threads;
-// dynamic shared memory 1024 + S * mma_stage_bytes(mpad of a full tile).
-// PRESPLIT: x comes split by xsplit_kernel (a.xs) and is copied by the
-// producer; otherwise the converter warps also split the stage's x (a.x).
+// grid = (ceil(N/128) * ks, tiles of x); cluster = (ks, 1, 1); 352 threads;
+// dynamic shared memory mma_smem_bytes(mpad of a full tile, a.RS).
+// PRESPLIT: x comes split by xsplit_kernel (a.xs) and is copied by warp 10;
+// otherwise the converter warps also split the block's x (a.x).
 template <int FMT, bool PRESPLIT>
 __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a) {
     namespace cg = cooperative_groups;
     extern __shared__ __align__(1024) uint8_t msm[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(msm);       // [S] stage loaded
-    uint64_t *conv = full + kMmaMaxStages;                   // [S] A operand written
-    uint64_t *empty = conv + kMmaMaxStages;                  // [S] stage's MMAs complete
-    uint64_t *done = empty + kMmaMaxStages;                  // every MMA complete
+    uint64_t *raw_full = reinterpret_cast<uint64_t *>(msm);
+    uint64_t *raw_empty = raw_full + kMmaMaxRaw;
+    uint64_t *b_full = raw_empty + kMmaMaxRaw;
+    uint64_t *a_full = b_full + kMmaMaxB;
+    uint64_t *mma_done = a_full + kMmaAStages;
+    uint64_t *done = mma_done + kMmaAStages;
     uint32_t *taddr_s = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_s = reinterpret_cast<volatile int *>(taddr_s + 1);
-    uint8_t *stages = msm + 1024;
+    uint8_t *bring = msm + 1024;
+    uint8_t *rawring = msm + a.raw_off;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = a.S;
+    const int RS = a.RS, BS = a.BS;
     const int rank = (int)(blockIdx.x % (unsigned)a.ks);
     const int64_t n0 = (int64_t)(blockIdx.x / (unsigned)a.ks) * kMmaRows;
     const int tile = (int)blockIdx.y + a.m_base / kMmaMaxN;
     const int m0 = tile * kMmaMaxN;
     const int mt = min(kMmaMaxN, a.M - m0);
     const int mpad = (mt + 15) & ~15;
-    const int sbytes = mma_stage_bytes<FMT>(mpad);
-    const int kb0 = (int)((int64_t)a.nkb * rank / a.ks);
-    const int nk = (int)((int64_t)a.nkb * (rank + 1) / a.ks) - kb0;
-    const uint32_t ncols = mma_tmem_cols(mpad);
-    constexpr int RAW = mma_raw_bytes<FMT>();
+    const int bbytes = 2 * mma_b_bytes(mpad);
+    // this CTA's K range: whole 256-wide slots sl0 .. sl0+nsl_c-1
+    const int sl0 = (int)((int64_t)a.nsl * rank / a.ks);
+    const int nsl_c = (int)((int64_t)a.nsl * (rank + 1) / a.ks) - sl0;
+    const int kb0 = sl0 * kMmaSub;
+    const int nk = min(a.nkb, (sl0 + nsl_c) * kMmaSub) - kb0;
+    constexpr int RAWG = mma_raw_group_bytes<FMT>();
+    // MMA issuers and the tensor-memory columns of each one's accumulator
+    const int NI = mpad <= 64 ? 4 : mpad <= 128 ? 2 : 1;
+    const uint32_t dcols = kMmaDCols / NI;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&conv[s], kMmaConvThreads);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < RS; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], kMmaConvThreads);
         }
-        mbar_init(done, 1);
+        for (int s = 0; s < BS; ++s) mbar_init(&b_full[s], PRESPLIT ? 1 : kMmaConvThreads);
+        for (int s = 0; s < kMmaAStages; ++s) {
+            mbar_init(&a_full[s], kMmaConvThreads);
+            mbar_init(&mma_done[s], NI);
+        }
+        mbar_init(done, NI);
         *abort_s = 0;
         fence_mbar_init();
     }
-    if (warp == 9) tmem_alloc(taddr_s, ncols);
+    if (warp == 9) tmem_alloc(taddr_s, kMmaTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *taddr_s;
 
     if (warp == 8) {
-        // ------------------------------------------------------------ producer
+        // ---------------------------------------------------- weight producer
         if (lane == 0) {
-            const uint8_t *xs_tile = a.xs + tile * mma_xs_tile_bytes(a.nkb);
-            const uint32_t bbytes = (uint32_t)(2 * mma_b_bytes(mpad));
             int issued = 0;
-            for (int j = 0; j < nk; ++j) {
-                const int s = j % S;
+            for (int u = 0; u < nsl_c; ++u) {
+                const int r = u % RS;
                 if (*abort_s) break;
-                if (j >= S && !mbar_wait(&empty[s], (uint32_t)(((j / S) - 1) & 1), kMmaWaitNs)) {
+                if (u >= RS && !mbar_wait(&raw_empty[r], (uint32_t)(((u / RS) - 1) & 1), kMmaWaitNs)) {
                     *abort_s = 1;
                     break;
                 }
-                uint8_t *st = stages + s * sbytes;
-                const int64_t kb = kb0 + j;
-                uint32_t bytes = PRESPLIT ? bbytes : 0u;
-                for (int g = 0; g < kMmaRows / kRowsPerGroup; ++g)
-                    bytes += raw_bytes_of<FMT>(a, n0 / kRowsPerGroup + g, kb);
-                mbar_arrive_expect_tx(&full[s], bytes);
+                uint8_t *slot = rawring + r * mma_raw_bytes<FMT>();
+                const int64_t gs = sl0 + u;
+                uint32_t bytes = 0;
                 for (int g = 0; g < kMmaRows / kRowsPerGroup; ++g) {
                     const int64_t gi = n0 / kRowsPerGroup + g;
-                    if (gi < a.groups)
-                        raw_copy<FMT>(a, gi, kb, st + g * mma_raw_group_bytes<FMT>(), &full[s]);
+                    if (gi < a.groups) bytes += raw_copy<FMT>(a, gi, gs, nullptr, nullptr);
                 }
-                if (PRESPLIT) {
-                    if (j == 0) pdl_wait();  // the split x comes from the kernel before
-                    bulk_g2s(st + RAW + 2 * mma_a_bytes(), xs_tile + kb * (int64_t)bbytes, bbytes,
-                             &full[s]);
+                mbar_arrive_expect_tx(&raw_full[r], bytes);
+                for (int g = 0; g < kMmaRows / kRowsPerGroup; ++g) {
+                    const int64_t gi = n0 / kRowsPerGroup + g;
+                    if (gi < a.groups) raw_copy<FMT>(a, gi, gs, slot + g * RAWG, &raw_full[r]);
                 }
+                issued = u + 1;
+            }
+            // copies still in flight after an abort land before the CTA exits
+            for (int u = issued - RS > 0 ? issued - RS : 0; u < issued; ++u)
+                mbar_wait(&raw_full[u % RS], (uint32_t)((u / RS) & 1), kMmaWaitNs);
+        }
+    } else if (warp == 10) {
+        // --------------------------------------------------------- x producer
+        if (PRESPLIT && lane == 0) {
+            const uint8_t *xs_tile = a.xs + tile * mma_xs_tile_bytes(a.nkb);
+            int issued = 0;
+            for (int j = 0; j < nk; ++j) {
+                const int s = j % BS, jp = j - BS;  // jp: the last block that used stage s
+                if (*abort_s) break;
+                if (jp >= 0 && !mbar_wait(&mma_done[jp % kMmaAStages],
+                                          (uint32_t)((jp / kMmaAStages) & 1), kMmaWaitNs)) {
+                    *abort_s = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&b_full[s], (uint32_t)bbytes);
+                if (j == 0) pdl_wait();  // the split x comes from the kernel before
+                bulk_g2s(bring + s * bbytes, xs_tile + (int64_t)(kb0 + j) * bbytes, (uint32_t)bbytes,
+                         &b_full[s]);
                 issued = j + 1;
             }
-            // copies still in flight after an abort finish before the CTA exits
-            for (int j = issued - S > 0 ? issued - S : 0; j < issued; ++j)
-                mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), kMmaWaitNs);
+            for (int j = issued - BS > 0 ? issued - BS : 0; j < issued; ++j)
+                mbar_wait(&b_full[j % BS], (uint32_t)((j / BS) & 1), kMmaWaitNs);
         }
-    } else if (warp == 9) {
-        // --------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+    } else if (warp == 9 || warp > 10) {
+        // -------------------------------------------------------- MMA issuers
+        const int iss = warp == 9 ? 0 : warp - 10;  // 0 .. 3
+        if (lane == 0 && iss < NI) {
             const uint32_t idesc = mma_idesc(mpad);
+            const uint32_t td = tmem + iss * dcols;
+            // descriptors advance by adding byte offsets / 16 to the address field
+            const uint64_t bdesc0 = smem_desc(smem_addr(bring));
+            const uint32_t b_lo16 = (uint32_t)mma_b_bytes(mpad) >> 4, kk16 = (uint32_t)(mpad * 32) >> 4;
             for (int j = 0; j < nk; ++j) {
-                const int s = j % S;
-                const uint32_t ph = (uint32_t)((j / S) & 1);
+                const int sa = j % kMmaAStages, sb = j % BS;
                 if (*abort_s) break;
-                if (!mbar_wait(&conv[s], ph, kMmaWaitNs) || !mbar_wait(&full[s], ph, kMmaWaitNs)) {
+                if (!mbar_wait(&a_full[sa], (uint32_t)((j / kMmaAStages) & 1), kMmaWaitNs) ||
+                    !mbar_wait(&b_full[sb], (uint32_t)((j / BS) & 1), kMmaWaitNs)) {
                     *abort_s = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sa_hi = smem_addr(stages + s * sbytes + RAW);
-                const uint32_t sa_lo = sa_hi + mma_a_bytes();
-                const uint32_t sb_hi = sa_lo + mma_a_bytes();
-                const uint32_t sb_lo = sb_hi + mma_b_bytes(mpad);
-#pragma unroll
-                for (int kk = 0; kk < kMmaKB / 16; ++kk) {
-                    const uint32_t ao = kk * (kMmaRows * 32), bo = kk * (mpad * 32);
-                    mma_bf16(tmem, smem_desc(sa_hi + ao), smem_desc(sb_hi + bo), idesc,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_bf16(tmem, smem_desc(sa_hi + ao), smem_desc(sb_lo + bo), idesc, 1u);
-                    mma_bf16(tmem, smem_desc(sa_lo + ao), smem_desc(sb_hi + bo), idesc, 1u);
+                const uint32_t ta_hi = tmem + kMmaDCols + sa * kMmaACols;
+                const uint32_t ta_lo = ta_hi + kMmaACols / 2;
+                const uint64_t bh = bdesc0 + ((uint32_t)(sb * bbytes) >> 4);
+                for (int kk = iss; kk < kMmaKB / 16; kk += NI) {
+                    const uint64_t dh = bh + kk * kk16, dl = dh + b_lo16;
+                    mma_bf16_ts(td, ta_hi + 8 * kk, dh, idesc, (j > 0 || kk > iss) ? 1u : 0u);
+                    mma_bf16_ts(td, ta_hi + 8 * kk, dl, idesc, 1u);
+                    mma_bf16_ts(td, ta_lo + 8 * kk, dh, idesc, 1u);
                 }
-                mma_commit(&empty[s]);
+                mma_commit(&mma_done[sa]);
             }
             mma_commit(done);  // arrives when every MMA issued above has completed
         }
@@ -465,67 +568,79 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
         const int g = row / kRowsPerGroup;
         const bool row_live = n0 / kRowsPerGroup + g < a.groups;
         const int64_t chunks = a.K / 32;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         for (int j = 0; j < nk; ++j) {
-            const int s = j % S;
+            const int u = j / kMmaSub, r = u % RS, sa = j % kMmaAStages;
             if (*abort_s) break;
-            if (!mbar_wait(&full[s], (uint32_t)((j / S) & 1), kMmaWaitNs)) {
+            if ((j % kMmaSub == 0 &&
+                 !mbar_wait(&raw_full[r], (uint32_t)((u / RS) & 1), kMmaWaitNs)) ||
+                (j >= kMmaAStages &&
+                 !mbar_wait(&mma_done[sa], (uint32_t)(((j / kMmaAStages) - 1) & 1), kMmaWaitNs))) {
                 *abort_s = 1;
                 break;
             }
-            uint8_t *st = stages + s * sbytes;
             const int64_t kb = kb0 + j;
             float w[32];
             if (row_live && 2 * kb + half < chunks) {
-                // scale slot of the chunk's block within its step
-                const int sidx = FMT == Q4_0 || FMT == Q8_0 ? (int)((2 * kb + half) & 7)
-                                 : FMT == I8_B64           ? (int)(kb & 7)
-                                                           : (int)((kb >> 2) & 7);
-                raw_chunk32<FMT>(st + g * mma_raw_group_bytes<FMT>() + (row % kRowsPerGroup) * kVec,
-                                 half, sidx, kb, mg, w);
+                raw_chunk32<FMT>(rawring + r * mma_raw_bytes<FMT>() + g * RAWG +
+                                     (row % kRowsPerGroup) * kVec,
+                                 half, kb, mg, w);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) w[i] = 0.f;
             }
-            uint8_t *a_hi = st + RAW;
+            // the block's 32 elements of this row -> A stage, columns 16*half ..
+            uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int k8 = 0; k8 < 4; ++k8) {
-                const uint32_t off = tile_off(kMmaRows, row, 32 * half + 8 * k8);
-                split_store8(w + 8 * k8, a_hi + off, a_hi + mma_a_bytes() + off);
-            }
+            for (int i = 0; i < 16; ++i) split2(w[2 * i], w[2 * i + 1], hi[i], lo[i]);
+            tc_fence_after();
+            const uint32_t ta = tmem + lane_base + kMmaDCols + sa * kMmaACols + 16 * half;
+            tmem_st16(ta, hi);
+            tmem_st16(ta + kMmaACols / 2, lo);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&a_full[sa]);
+            if (j % kMmaSub == kMmaSub - 1 || j == nk - 1) mbar_arrive(&raw_empty[r]);
             if (!PRESPLIT) {
-                // x of the stage: item i = (row m = i % mpad, 8-wide piece i / mpad);
+                // x of the block: item i = (row m = i % mpad, 8-wide piece i / mpad);
                 // all loads first, then the splits
+                const int sb = j % BS, jp = j - BS;  // jp: the last block that used stage sb
+                if (jp >= 0 && !mbar_wait(&mma_done[jp % kMmaAStages],
+                                          (uint32_t)((jp / kMmaAStages) & 1), kMmaWaitNs)) {
+                    *abort_s = 1;
+                    break;
+                }
                 if (j == 0) pdl_wait();  // x may come from the previous kernel on the stream
                 constexpr int XI = kMmaMaxN * 8 / kMmaConvThreads;
-                uint8_t *b_hi = a_hi + 2 * mma_a_bytes();
+                uint8_t *b_hi = bring + sb * bbytes;
                 float4 xv[XI][2];
 #pragma unroll
-                for (int u = 0; u < XI; ++u) {
-                    const int i = (int)threadIdx.x + u * kMmaConvThreads;
+                for (int q = 0; q < XI; ++q) {
+                    const int i = (int)threadIdx.x + q * kMmaConvThreads;
                     const int m = i % mpad;
                     const int64_t k = kb * kMmaKB + 8 * (i / mpad);
                     if (i < mpad * 8 && m < mt && k < a.K) {
                         const float *src = a.x + (int64_t)(m0 + m) * a.K + k;
-                        xv[u][0] = __ldg(reinterpret_cast<const float4 *>(src));
-                        xv[u][1] = __ldg(reinterpret_cast<const float4 *>(src + 4));
+                        xv[q][0] = __ldg(reinterpret_cast<const float4 *>(src));
+                        xv[q][1] = __ldg(reinterpret_cast<const float4 *>(src + 4));
                     } else {
-                        xv[u][0] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        xv[u][1] = xv[u][0];
+                        xv[q][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        xv[q][1] = xv[q][0];
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < XI; ++u) {
-                    const int i = (int)threadIdx.x + u * kMmaConvThreads;
+                for (int q = 0; q < XI; ++q) {
+                    const int i = (int)threadIdx.x + q * kMmaConvThreads;
                     if (i < mpad * 8) {
-                        const float v[8] = {xv[u][0].x, xv[u][0].y, xv[u][0].z, xv[u][0].w,
-                                            xv[u][1].x, xv[u][1].y, xv[u][1].z, xv[u][1].w};
+                        const float v[8] = {xv[q][0].x, xv[q][0].y, xv[q][0].z, xv[q][0].w,
+                                            xv[q][1].x, xv[q][1].y, xv[q][1].z, xv[q][1].w};
                         const uint32_t off = tile_off(mpad, i % mpad, 8 * (i / mpad));
                         split_store8(v, b_hi + off, b_hi + mma_b_bytes(mpad) + off);
                     }
                 }
+                fence_async_smem();  // the tensor cores read what the generic proxy wrote
+                mbar_arrive(&b_full[sb]);
             }
-            fence_async_smem();  // the tensor cores read what the generic proxy wrote
-            mbar_arrive(&conv[s]);
         }
     }
 
@@ -547,12 +662,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
         if (warp < 8) {
             for (int c0 = 32 * (warp >> 2); c0 < mpad; c0 += 64) {
                 uint32_t r[32];
-                if (have) {
-                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = 0u;
-                }
+                tmem_sum32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, NI, dcols, have, r);
                 if (nq < a.N) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -562,18 +672,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
             }
         }
     } else {
-        // partial D of this CTA into shared memory, P[m][row] (the stages are
+        // partial D of this CTA into shared memory, P[m][row] (the rings are
         // free: every MMA has completed and every copy has landed)
-        float *P = reinterpret_cast<float *>(stages);
+        float *P = reinterpret_cast<float *>(bring);
         if (warp < 8) {
             for (int c0 = 32 * (warp >> 2); c0 < mpad; c0 += 64) {
                 uint32_t r[32];
-                if (have) {
-                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = 0u;
-                }
+                tmem_sum32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, NI, dcols, have, r);
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     if (c0 + i < mpad) P[(c0 + i) * kMmaRows + 32 * q + lane] = __uint_as_float(r[i]);
@@ -621,7 +726,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) tmem_dealloc(tmem, ncols);
+    if (warp == 9) tmem_dealloc(tmem, kMmaTmemCols);
 }
 
 }  // namespace lean

@@ -33,6 +33,7 @@ SIGNATURES = {
     "lean_qmatmul": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "lean_qmatmul_ex": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp]),
     "lean_qmatmul_workspace_bytes": (_i64, [_int, _i64, _i64, _i64]),
+    "lean_tensor_core_min_m": (_int, []),
     "lean_qmatmul_ws": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp, _i64,
                                _vp]),
     "lean_batch_workspace_bytes": (_i64, [_int, _int, _vp]),
@@ -172,6 +173,11 @@ def lean_qmatmul_ex(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int
 
 def lean_qmatmul_workspace_bytes(fmt: int, N: int, K: int, M: int) -> int:
     return _lib.lean_qmatmul_workspace_bytes(fmt, N, K, M)
+
+
+def lean_tensor_core_min_m() -> int:
+    """Rows of x from which the product runs on the tensor cores."""
+    return _lib.lean_tensor_core_min_m()
 
 
 def lean_qmatmul_ws(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,

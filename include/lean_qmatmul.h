@@ -121,8 +121,9 @@ lean_status lean_dequant(int fmt, const void *W_packed_dev, float *w_dev,
  *   x_dev         device, 16-byte aligned, x[M][K] fp32 row-major (read only)
  *   y_dev         device, 4-byte aligned, y[M][N] fp32 row-major, overwritten
  *   stream        cudaStream_t as void*
- * M = 1 is the decode GEMV; M = 2..31 runs on the CUDA cores with each
- * decoded weight reused M times; M >= 32 runs on the tcgen05 tensor cores
+ * M = 1 is the decode GEMV; M = 2..15 runs on the CUDA cores with each
+ * decoded weight reused M times; M >= 16 (lean_tensor_core_min_m()) runs on
+ * the tcgen05 tensor cores
  * with split-bf16 operands (w = w_hi + w_lo, x = x_hi + x_lo, three MMAs into
  * fp32 accumulators), every format.  Accuracy: |y - y_exact| <= 1e-4 *
  * sum_k |w x| + 1e-6 per element.  Nothing is allocated: without a workspace
@@ -149,9 +150,12 @@ lean_status lean_qmatmul_ex(int fmt, const void *W_packed_dev, const float *x_de
                             float *y_dev, int64_t N, int64_t K, int64_t M,
                             unsigned flags, void *stream);
 
+/* Rows of x from which lean_qmatmul uses the tensor cores (16). */
+int lean_tensor_core_min_m(void);
+
 /* Bytes of device workspace that lean_qmatmul_ws uses for this shape (0 when
- * it uses none: M = 2..31), or -1 on a bad fmt or shape.  M = 1: stream-K
- * partial sums and counters.  M >= 32: x split into bf16 hi / lo operand
+ * it uses none: M = 2..15), or -1 on a bad fmt or shape.  M = 1: stream-K
+ * partial sums and counters.  M >= 16: x split into bf16 hi / lo operand
  * tiles, 4 bytes per element of x with M padded to 16 per 256-row tile and K
  * to 64. */
 int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);
@@ -165,12 +169,12 @@ int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);
  *   workspace        device, 256-byte aligned, >= lean_qmatmul_workspace_bytes
  *                    bytes.  M = 1: it must be zeroed once (cudaMemset) before
  *                    its first use, and every call leaves it zeroed again.
- *                    M >= 32: any contents; a first kernel writes x there as
+ *                    M >= 16: any contents; a first kernel writes x there as
  *                    bf16 hi / lo operand tiles, once for all CTAs, which the
  *                    product then copies with TMA (the fast path for large M).
  *   workspace_bytes  its size (LEAN_ERR_SHAPE if too small).
  * Calls that may run at the same time on the GPU must not share a workspace.
- * The workspace is ignored for M = 2..31. */
+ * The workspace is ignored for M = 2..15. */
 lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_dev,
                             float *y_dev, int64_t N, int64_t K, int64_t M,
                             unsigned flags, void *workspace, int64_t workspace_bytes,

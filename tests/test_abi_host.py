@@ -57,11 +57,13 @@ def test_sizes(lean):
 
 
 def test_workspace_sizes(lean):
-    """M = 1: stream-K scratch; 2..31 rows: none; 32 rows and up: x split
+    """M = 1: stream-K scratch; 2..15 rows: none; 16 rows and up: x split
     into bf16 hi + lo (4 bytes per element) over rows padded to 16 within each
     256-row tile and K padded to 64."""
     assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 1) > 0
-    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 31) == 0
+    assert lean.lean_tensor_core_min_m() == 16
+    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 15) == 0
+    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 16) == 16 * 960 * 4
     assert lean.lean_qmatmul_workspace_bytes(0, 2048, 2048, 256) == 256 * 2048 * 4
     assert lean.lean_qmatmul_workspace_bytes(0, 2048, 2048, 32) == 32 * 2048 * 4
     assert lean.lean_qmatmul_workspace_bytes(0, 100, 96, 33) == 48 * 128 * 4
