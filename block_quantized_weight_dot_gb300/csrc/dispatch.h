@@ -25,18 +25,24 @@ struct HostProb {
 };
 
 // Workspace of the balanced (stream-K) GEMV: per-CTA partial sums of the row
-// groups split between CTAs (two sides x 16 groups x 32 rows), then one
-// arrival counter per row group.
+// groups split between CTAs (two sides x 16 groups x 32 rows), then x as
+// integer planes (xq_bytes, may be 0), then one arrival counter per row group.
 struct WorkspaceLayout {
-    int64_t part_off, cnt_off, total;
+    int64_t part_off, xq_off, cnt_off, total;
 };
-inline WorkspaceLayout workspace_layout(int64_t groups) {
+inline WorkspaceLayout workspace_layout(int64_t groups, int64_t xq_bytes = 0) {
     WorkspaceLayout w;
     w.part_off = 0;
-    w.cnt_off = (int64_t)kMaxStreamCtas * 2 * 16 * 32 * 4;
-    w.total = (w.cnt_off + groups * 4 + 255) / 256 * 256;
+    w.xq_off = (int64_t)kMaxStreamCtas * 2 * 16 * 32 * 4;
+    w.cnt_off = w.xq_off + (xq_bytes + 255) / 256 * 256;
+    w.total = w.cnt_off + (groups * 4 + 255) / 256 * 256;
     return w;
 }
+// x planes pay for their extra launch only when the call streams this many
+// weight bytes or more (a single mid-size GEMV is bound by launch latency)
+constexpr int64_t kPlanesMinWeightBytes = (int64_t)32 << 20;
+// bytes of the x planes of one M = 1 product (0 for Q6_K, which takes fp32 x)
+inline int64_t xq_bytes(int fmt, int64_t K) { return fmt == Q6_K ? 0 : K / 32 * kXqBlockBytes; }
 
 template <int FMT>
 lean_status simt_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
@@ -47,8 +53,15 @@ template <int FMT>
 lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
                     unsigned flags, void *ws, int64_t ws_bytes, unsigned *err,
                     cudaStream_t stream);
+// planes: with a workspace, hand x to the integer formats as planes (dp4a)
 template <int FMT>
 lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
-                       unsigned *err, cudaStream_t stream);
+                       bool planes, unsigned *err, cudaStream_t stream);
+
+// The M = 1 product with a workspace; planes = false keeps x in fp32 (the
+// layout without a plane region, as the fixed array of lean_qmatmul_fixed_ws).
+lean_status qmatmul_m1_ws(int fmt, const void *W, const float *x, float *y, int64_t N,
+                          int64_t K, unsigned flags, void *ws, int64_t ws_bytes, bool planes,
+                          cudaStream_t stream);
 
 }  // namespace lean

@@ -296,7 +296,7 @@ inline bool stream_totals(const HostProb *ph, int n, int64_t *groups) {
 
 template <int FMT, int NP>
 lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
-                          unsigned *err, cudaStream_t stream) {
+                          bool planes, unsigned *err, cudaStream_t stream) {
     using C = StreamCfg<FMT>;
     using L = StreamLayout<FMT>;
     static std::atomic<uint64_t> smem_done{0};
@@ -322,6 +322,7 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
         p.unit0 = units;
         p.gblock0 = gblocks;
         p.group0 = groups;
+        p.xq0 = 0;
         units += p.gblocks * p.chunks;
         gblocks += p.gblocks;
         groups += g.groups;
@@ -330,14 +331,54 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
     a.total_gblocks = gblocks;
     a.mg = make_magic();
     a.err = err;
+    a.xq = nullptr;
     const int64_t slots = std::min<int64_t>((int64_t)sm_count() * C::CPS, kMaxStreamCtas);
+    unsigned kflags = flags;
     if (ws != nullptr) {
-        const WorkspaceLayout wl = workspace_layout(groups);
+        // room for the x planes of every problem, back to back (the layout is
+        // the one lean_*_workspace_bytes describe, planes used or not)
+        int64_t xqb = 0, wbytes = 0;
+        int max_nb = 0;
+        if (planes && XPlanes<FMT>::on) {
+            for (int i = 0; i < n; ++i) {
+                a.p[i].xq0 = xqb;
+                xqb += xq_bytes(FMT, ph[i].g.K);
+                wbytes += ph[i].g.total;
+                max_nb = std::max<int>(max_nb, (int)(ph[i].g.K / 32));
+            }
+        }
+        const bool use_planes =
+            xqb > 0 && (wbytes >= kPlanesMinWeightBytes || (flags & LEAN_FLAG_X_PLANES));
+        const WorkspaceLayout wl = workspace_layout(groups, xqb);
         if (ws_bytes < wl.total) return LEAN_ERR_SHAPE;
         a.balanced = 1;
         a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, units));
         a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + wl.part_off);
         a.cnt = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + wl.cnt_off);
+        if (use_planes) {
+            XprepArgs<NP> xa;
+            xa.nprob = n;
+            xa.pad = 0;
+            xa.xq = static_cast<uint8_t *>(ws) + wl.xq_off;
+            for (int i = 0; i < n; ++i) {
+                xa.p[i].x = ph[i].x;
+                xa.p[i].xq0 = a.p[i].xq0;
+                xa.p[i].nb = (int)(ph[i].g.K / 32);
+                xa.p[i].pad = 0;
+            }
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)((max_nb + 7) / 8), (unsigned)n, 1);
+            cfg.blockDim = dim3(256, 1, 1);
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[2];
+            fill_launch(cfg, attr, 1, flags);
+            if (cudaLaunchKernelEx(&cfg, xprep_kernel<FMT, NP>, xa) != cudaSuccess)
+                return LEAN_ERR_CUDA;
+            a.xq = xa.xq;
+            // after the plane kernel (which itself starts only when the caller's
+            // flags allow) the product is always launched programmatically
+            kflags = LEAN_FLAG_EARLY_WEIGHTS;
+        }
     } else {
         a.balanced = 0;
         a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, gblocks));
@@ -352,17 +393,17 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
-    fill_launch(cfg, attr, 1, flags);
+    fill_launch(cfg, attr, 1, kflags);
     return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
 }
 
 template <int FMT>
 lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
-                       unsigned *err, cudaStream_t stream) {
+                       bool planes, unsigned *err, cudaStream_t stream) {
     int64_t groups;
     if (!stream_totals(ph, n, &groups)) return LEAN_ERR_SHAPE;
-    if (n == 1) return launch_stream<FMT, 1>(ph, n, flags, ws, ws_bytes, err, stream);
-    return launch_stream<FMT, kMaxBatch>(ph, n, flags, ws, ws_bytes, err, stream);
+    if (n == 1) return launch_stream<FMT, 1>(ph, n, flags, ws, ws_bytes, planes, err, stream);
+    return launch_stream<FMT, kMaxBatch>(ph, n, flags, ws, ws_bytes, planes, err, stream);
 }
 
 }  // namespace lean
@@ -373,7 +414,7 @@ lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int6
                                        int64_t, unsigned, cudaStream_t);                       \
     template lean_status dequant_fmt<FMT>(const Geom &, const uint8_t *, float *, cudaStream_t); \
     template lean_status stream_fmt<FMT>(const HostProb *, int, unsigned, void *, int64_t,     \
-                                         unsigned *, cudaStream_t);                            \
+                                         bool, unsigned *, cudaStream_t);                      \
     template lean_status mma_fmt<FMT>(const Geom &, const uint8_t *, const float *, float *,   \
                                       int64_t, unsigned, void *, int64_t, unsigned *,          \
                                       cudaStream_t);

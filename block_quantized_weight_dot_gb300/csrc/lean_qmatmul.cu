@@ -37,19 +37,19 @@ unsigned *error_word() {
 
 template <int FMT>
 lean_status run_stream(const HostProb *ph, int n, unsigned flags, void *ws, int64_t wsb,
-                       cudaStream_t s) {
+                       bool planes, cudaStream_t s) {
     unsigned *err = error_word();
     if (!err) return LEAN_ERR_CUDA;
-    return stream_fmt<FMT>(ph, n, flags, ws, wsb, err, s);
+    return stream_fmt<FMT>(ph, n, flags, ws, wsb, planes, err, s);
 }
 
 lean_status dispatch_stream(int fmt, const HostProb *ph, int n, unsigned flags, void *ws,
-                            int64_t wsb, cudaStream_t s) {
+                            int64_t wsb, bool planes, cudaStream_t s) {
     switch (fmt) {
-    case LEAN_Q4_0: return run_stream<Q4_0>(ph, n, flags, ws, wsb, s);
-    case LEAN_Q8_0: return run_stream<Q8_0>(ph, n, flags, ws, wsb, s);
-    case LEAN_I8_B64: return run_stream<I8_B64>(ph, n, flags, ws, wsb, s);
-    case LEAN_Q6_K: return run_stream<Q6_K>(ph, n, flags, ws, wsb, s);
+    case LEAN_Q4_0: return run_stream<Q4_0>(ph, n, flags, ws, wsb, planes, s);
+    case LEAN_Q8_0: return run_stream<Q8_0>(ph, n, flags, ws, wsb, planes, s);
+    case LEAN_I8_B64: return run_stream<I8_B64>(ph, n, flags, ws, wsb, planes, s);
+    case LEAN_Q6_K: return run_stream<Q6_K>(ph, n, flags, ws, wsb, planes, s);
     }
     return LEAN_ERR_FORMAT;
 }
@@ -61,11 +61,25 @@ lean_status check_product(int fmt, const void *W, const float *x, const float *y
     if (M > ((int64_t)1 << 31) / std::max<int64_t>(K, N)) return LEAN_ERR_SHAPE;
     if (!W || !x || !y) return LEAN_ERR_NULL;
     if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return LEAN_ERR_ALIGN;
-    if (flags & ~(unsigned)LEAN_FLAG_EARLY_WEIGHTS) return LEAN_ERR_FORMAT;
+    if (flags & ~(unsigned)(LEAN_FLAG_EARLY_WEIGHTS | LEAN_FLAG_X_PLANES)) return LEAN_ERR_FORMAT;
     return LEAN_OK;
 }
 
 }  // namespace
+
+namespace lean {
+lean_status qmatmul_m1_ws(int fmt, const void *W, const float *x, float *y, int64_t N,
+                          int64_t K, unsigned flags, void *ws, int64_t ws_bytes, bool planes,
+                          cudaStream_t stream) {
+    Geom g;
+    lean_status st = check_product(fmt, W, x, y, N, K, 1, flags, &g);
+    if (st != LEAN_OK) return st;
+    if (ws && !aligned(ws, 256)) return LEAN_ERR_ALIGN;
+    cudaGetLastError();
+    HostProb hp = {(const uint8_t *)W, x, y, g};
+    return dispatch_stream(fmt, &hp, 1, flags, ws, ws_bytes, planes, stream);
+}
+}  // namespace lean
 
 extern "C" {
 
@@ -81,7 +95,7 @@ lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_de
     cudaStream_t s = (cudaStream_t)stream;
     if (M == 1) {
         HostProb hp = {W, x_dev, y_dev, g};
-        return dispatch_stream(fmt, &hp, 1, flags, workspace, workspace_bytes, s);
+        return dispatch_stream(fmt, &hp, 1, flags, workspace, workspace_bytes, true, s);
     }
     if (M >= kMmaMinM) {
         unsigned *err = error_word();
@@ -122,18 +136,19 @@ int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M) {
     if (M <= 0 || !make_geom(fmt, N, K, &g)) return -1;
     if (M >= kMmaMinM) return mma_xs_bytes(M, K);
     if (M > 1) return 0;
-    return workspace_layout(g.groups).total;
+    return workspace_layout(g.groups, xq_bytes(fmt, K)).total;
 }
 
 int64_t lean_batch_workspace_bytes(int fmt, int count, const lean_problem *problems) {
     if (count < 1 || count > LEAN_MAX_BATCH || !problems) return -1;
-    int64_t groups = 0;
+    int64_t groups = 0, xqb = 0;
     for (int i = 0; i < count; ++i) {
         Geom g;
         if (!make_geom(fmt, problems[i].N, problems[i].K, &g)) return -1;
         groups += g.groups;
+        xqb += xq_bytes(fmt, problems[i].K);
     }
-    return workspace_layout(groups).total;
+    return workspace_layout(groups, xqb).total;
 }
 
 lean_status lean_qmatmul_batch(int fmt, int count, const lean_problem *problems, unsigned flags,
@@ -152,7 +167,7 @@ lean_status lean_qmatmul_batch(int fmt, int count, const lean_problem *problems,
         hp[i].y = p.y;
     }
     cudaGetLastError();
-    return dispatch_stream(fmt, hp, count, flags, workspace, workspace_bytes,
+    return dispatch_stream(fmt, hp, count, flags, workspace, workspace_bytes, true,
                            (cudaStream_t)stream);
 }
 

@@ -66,7 +66,9 @@ lean_status lean_qmatmul_fixed_ws(int fmt, const void *W_packed_dev, const float
     if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + wl.cnt_off, 0, (size_t)(g.groups * 4),
                         (cudaStream_t)stream) != cudaSuccess)
         return LEAN_ERR_CUDA;
-    return lean_qmatmul_ws(fmt, W_packed_dev, x_dev, y_dev, N, K, 1, flags, ws, wl.total, stream);
+    // x stays fp32 here: the array has no room for the x planes of every K
+    return qmatmul_m1_ws(fmt, W_packed_dev, x_dev, y_dev, N, K, flags, ws, wl.total, false,
+                         (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -7,9 +7,22 @@
 //  - work is cut into units: one chunk of K (BPC blocks of one step) for each
 //    of 8 consecutive 32-row groups of one matrix.  A producer lane copies a
 //    unit -- the 8 groups' quant vectors of the chunk with their scale vector,
-//    and the chunk's slice of x once for all 8 -- into a shared-memory slot
-//    with bulk asynchronous copies (cp.async.bulk), counting the bytes on the
-//    slot's mbarrier;
+//    and the chunk's x once for all 8 -- into a shared-memory slot with bulk
+//    asynchronous copies (cp.async.bulk), counting the bytes on the slot's
+//    mbarrier;
+//  - with a workspace, the integer formats (Q4_0, Q8_0, I8_B64) take x as
+//    integer planes written once per call by xprep_kernel, so that the dot
+//    products run on dp4a: each 32-element block of x is
+//    scaled by a power of two 2^s chosen from its largest magnitude, rounded
+//    to integers X with |X| <= 2^22, and cut into three byte planes
+//    X = X2*2^16 + X1*2^8 + X0 (X2 signed).  Every plane's dp4a sum starts at
+//    -offset * (sum of the plane) (offset 8 for Q4_0, 128 for the stored int8
+//    bytes), so it ends as the exact integer sum of (q - offset) * plane; the
+//    three sums combine in fp32 and scale by d * 2^-s.  The rounding of x is
+//    at most 2^-23 of the block's largest |x|; a block of x = e_k stays exact.
+//    Without a workspace, and for Q6_K (whose 6-bit fields do not come out
+//    as bytes cheaply), x stays fp32 and the decode is the exact
+//    mantissa-bias conversion with paired fp32 FMAs;
 //  - consumer warp w owns group w of every unit: lane r decodes row r from
 //    shared memory (conflict-free 16-byte reads, x as a broadcast read) and
 //    keeps the group's running sum in a register across units, so no warp
@@ -60,6 +73,7 @@ struct StreamProb {
     int64_t gblocks;         // group blocks (8 groups each)
     int64_t unit0, gblock0;  // first global unit / group block of this problem
     int64_t group0;          // first global group
+    int64_t xq0;             // byte offset of this problem's x planes in xq
 };
 
 template <int NP>
@@ -72,6 +86,7 @@ struct StreamArgs {
     float *part;    // [ctas][2][8][32] partial sums of groups split between CTAs
     unsigned *cnt;  // [total groups] arrival counters, all zero between calls
     unsigned *err;  // device error word (bits of StreamError)
+    const uint8_t *xq;  // x as planes (xprep_kernel), or null: fp32 x
     Magic mg;
     StreamProb p[NP];
 };
@@ -101,6 +116,13 @@ template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, BPC = 4, E = 
 template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, BPC = 2, E = 64, S = 2, CPS = 2, GPW = 1; };
 template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, BPC = 1, E = 256, S = 3, CPS = 1, GPW = 1; };
 
+// x as integer planes (dp4a) for the integer formats
+template <int FMT> struct XPlanes { static constexpr bool on = FMT != Q6_K; };
+// One 32-element block of x in plane form: {init2, init1, init0, 2^-s} then
+// plane 2 (signed bytes), plane 1, plane 0, 32 bytes each.
+constexpr int kXqBytes = kXqBlockBytes;
+static_assert(kXqBytes == 16 + 3 * 32, "header + three planes");
+
 template <int FMT>
 struct StreamLayout {
     using C = StreamCfg<FMT>;
@@ -108,7 +130,7 @@ struct StreamLayout {
     static constexpr int CHUNK_BYTES = (C::BPC * C::VPB + 1) * kVecBytes;  // one group's chunk
     static constexpr int XE = C::BPC * C::E;                           // x elements of a unit
     static constexpr int GPU = kStreamWarps * C::GPW;                  // row groups of a unit
-    static constexpr int SLOT_BYTES = GPU * CHUNK_BYTES + XE * 4;
+    static constexpr int SLOT_BYTES = GPU * CHUNK_BYTES + XE * 4;  // planes take less than fp32
     // shared memory: [full S][empty S][abort][pad][ring S*SLOT]
     static constexpr int OFF_FULL = 0;
     static constexpr int OFF_EMPTY = 8 * C::S;
@@ -177,6 +199,126 @@ __device__ __forceinline__ ChunkPos chunk_pos(const StreamProb &p, int c) {
     q.nblk = q.s == p.steps - 1 ? p.last_blocks : 8;
     q.nbc = min(C::BPC, q.nblk - q.sub * C::BPC);
     return q;
+}
+
+// ---- x as integer planes ------------------------------------------------------
+// Byte of element l (0..31) of a block in its planes: Q4_0 words hold the
+// even elements of a weight word (its low nibbles) then the odd ones (high
+// nibbles); the int8 formats keep element order.
+template <int FMT>
+__device__ __forceinline__ int plane_pos(int l) {
+    if (FMT == Q4_0) return 4 * (2 * (l >> 3) + (l & 1)) + ((l & 7) >> 1);
+    return l;
+}
+// The warp converts one block of 32 elements of x (global) into its planes
+// at dst; lane l handles element l.
+template <int FMT>
+__device__ __forceinline__ void x_block_to_planes(const float *xs, uint8_t *dst, int lane) {
+    constexpr int OFF = FMT == Q4_0 ? 8 : 128;
+    const float v = xs[lane];
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
+    // |x| * 2^s <= 2^22 for the block's largest |x| (s capped for tiny blocks)
+    const int s = min(21 - ((int)(mx >> 23) - 127), 126);
+    const int X = __float2int_rn(v * __int_as_float((127 + s) << 23));
+    const int x0 = X & 255, x1 = (X >> 8) & 255, x2 = X >> 16;
+    const int pos = plane_pos<FMT>(lane);
+    dst[16 + pos] = (uint8_t)x2;
+    dst[48 + pos] = (uint8_t)x1;
+    dst[80 + pos] = (uint8_t)x0;
+    const int s2 = __reduce_add_sync(0xffffffffu, x2);
+    const int s1 = __reduce_add_sync(0xffffffffu, x1);
+    const int s0 = __reduce_add_sync(0xffffffffu, x0);
+    if (lane == 0) {
+        // a block holding Inf or NaN gives NaN
+        const float inv =
+            mx >= 0x7f800000u ? __int_as_float(0x7fc00000) : __int_as_float((127 - s) << 23);
+        *reinterpret_cast<int4 *>(dst) = make_int4(-OFF * s2, -OFF * s1, -OFF * s0, __float_as_int(inv));
+    }
+}
+
+// x of several problems as planes: blockIdx.y = problem, one warp per block
+// of 32 elements.  xq + p.xq0 receives the problem's K/32 plane blocks.
+struct XprepProb {
+    const float *x;
+    int64_t xq0;
+    int nb;  // blocks of 32 elements
+    int pad;
+};
+template <int NP>
+struct XprepArgs {
+    int nprob;
+    int pad;
+    uint8_t *xq;
+    XprepProb p[NP];
+};
+template <int FMT, int NP>
+__global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ XprepArgs<NP> a) {
+    pdl_launch_dependents();
+    pdl_wait();  // x may come from the previous kernel on the stream
+    const XprepProb &p = a.p[blockIdx.y];
+    const int b = (int)blockIdx.x * 8 + (int)(threadIdx.x >> 5);
+    if (b >= p.nb) return;
+    x_block_to_planes<FMT>(p.x + 32 * (int64_t)b, a.xq + p.xq0 + (int64_t)b * kXqBytes,
+                           (int)(threadIdx.x & 31));
+}
+
+__device__ __forceinline__ uint32_t dp4a_us(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// sum over one x block of (q - offset) * x, times 2^s; q bytes in w[0..7]
+// (four per word, in the block's plane order)
+__device__ __forceinline__ float plane_dot(const uint32_t (&w)[8], const uint8_t *xq) {
+    const int4 h = *reinterpret_cast<const int4 *>(xq);
+    const uint4 a2 = *reinterpret_cast<const uint4 *>(xq + 16), b2 = *reinterpret_cast<const uint4 *>(xq + 32);
+    const uint4 a1 = *reinterpret_cast<const uint4 *>(xq + 48), b1 = *reinterpret_cast<const uint4 *>(xq + 64);
+    const uint4 a0 = *reinterpret_cast<const uint4 *>(xq + 80), b0 = *reinterpret_cast<const uint4 *>(xq + 96);
+    const uint32_t P2[8] = {a2.x, a2.y, a2.z, a2.w, b2.x, b2.y, b2.z, b2.w};
+    const uint32_t P1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
+    const uint32_t P0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
+    uint32_t s2 = (uint32_t)h.x, s1 = (uint32_t)h.y, s0 = (uint32_t)h.z;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        s2 = dp4a_us(w[i], P2[i], s2);
+        s1 = dp4a_uu(w[i], P1[i], s1);
+        s0 = dp4a_uu(w[i], P0[i], s0);
+    }
+    const float T = fmaf((float)(int)s2, 65536.f, fmaf((float)(int)s1, 256.f, (float)(int)s0));
+    return __int_as_float(h.w) * T;
+}
+// One block with x as planes: this lane's row, block b of the step at ws, x
+// planes of the chunk at xq.
+template <int FMT>
+__device__ __forceinline__ float block_dot_q(const uint8_t *ws, const uint8_t *xq, int b, float d,
+                                             int lane) {
+    using C = StreamCfg<FMT>;
+    if (FMT == Q4_0) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(ws + b * kVecBytes + lane * 16);
+        uint32_t w[8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint32_t x = word_of(v, t);
+            w[2 * t] = x & 0x0F0F0F0Fu;
+            w[2 * t + 1] = (x >> 4) & 0x0F0F0F0Fu;
+        }
+        return d * plane_dot(w, xq + b * kXqBytes);
+    } else {  // Q8_0 (one x block) or I8_B64 (two): stored bytes q + 128
+        float r = 0.f;
+#pragma unroll
+        for (int h = 0; h < C::E / 32; ++h) {
+            const uint4 va = *reinterpret_cast<const uint4 *>(ws + (b * C::VPB + 2 * h) * kVecBytes + lane * 16);
+            const uint4 vb = *reinterpret_cast<const uint4 *>(ws + (b * C::VPB + 2 * h + 1) * kVecBytes + lane * 16);
+            const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+            r += plane_dot(w, xq + (b * (C::E / 32) + h) * kXqBytes);
+        }
+        return d * r;
+    }
 }
 
 // ---- per-format consumer work on one chunk held in shared memory ------------
@@ -260,10 +402,23 @@ __device__ __forceinline__ float block_dot(const uint8_t *ws, const float *xb, i
 // chunk's x; sub: the chunk's place in its step (for the scale slots).
 template <int FMT>
 __device__ __forceinline__ float consume_chunk(const uint8_t *ws, const float *xs, int nbc, int sub,
-                                               int lane, const Magic &mg) {
+                                               int lane, const Magic &mg, bool planes) {
     using C = StreamCfg<FMT>;
     const uint4 sv = *reinterpret_cast<const uint4 *>(ws + nbc * C::VPB * kVecBytes + lane * 16);
     float acc = 0.f;
+    if (XPlanes<FMT>::on && planes) {
+        const uint8_t *xq = reinterpret_cast<const uint8_t *>(xs);
+        if (nbc == C::BPC) {
+#pragma unroll
+            for (int i = 0; i < C::BPC; ++i)
+                acc += block_dot_q<FMT>(ws, xq, i, scale_of(sv, sub * C::BPC + i), lane);
+        } else {
+#pragma unroll
+            for (int i = 0; i < C::BPC; ++i)
+                if (i < nbc) acc += block_dot_q<FMT>(ws, xq, i, scale_of(sv, sub * C::BPC + i), lane);
+        }
+        return acc;
+    }
     if (nbc == C::BPC) {
 #pragma unroll
         for (int i = 0; i < C::BPC; ++i)
@@ -313,12 +468,12 @@ __device__ __forceinline__ void q4_block_rows(const uint8_t *ws, int stride, con
 // kStreamWarps chunks apart in the slot.
 template <int FMT>
 __device__ __forceinline__ void consume_rows(const uint8_t *ws, const float *xs, int nbc, int sub,
-                                             int nlive, int lane, const Magic &mg,
+                                             int nlive, int lane, const Magic &mg, bool planes,
                                              float (&acc)[StreamCfg<FMT>::GPW]) {
     using C = StreamCfg<FMT>;
     using L = StreamLayout<FMT>;
     constexpr int stride = kStreamWarps * L::CHUNK_BYTES;
-    if (FMT == Q4_0 && C::GPW > 1 && nlive == C::GPW) {
+    if (FMT == Q4_0 && C::GPW > 1 && nlive == C::GPW && !planes) {
         uint4 sv[C::GPW];
 #pragma unroll
         for (int r = 0; r < C::GPW; ++r)
@@ -347,7 +502,7 @@ __device__ __forceinline__ void consume_rows(const uint8_t *ws, const float *xs,
     }
 #pragma unroll
     for (int r = 0; r < C::GPW; ++r)
-        if (r < nlive) acc[r] += consume_chunk<FMT>(ws + r * stride, xs, nbc, sub, lane, mg);
+        if (r < nlive) acc[r] += consume_chunk<FMT>(ws + r * stride, xs, nbc, sub, lane, mg, planes);
 }
 
 template <int FMT, int NP>
@@ -403,19 +558,26 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     if (warp == kStreamWarps) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        const float *xsrc[C::S];
+        const bool planes = XPlanes<FMT>::on && a.xq != nullptr;
+        const uint8_t *xsrc[C::S];
         uint32_t xbytes[C::S];
         // arm slot j's barrier for the whole unit and copy the weights; returns
-        // the x source through xs / xb for a later copy
-        auto issue_weights = [&](int64_t j, const float *&xs, uint32_t &xb) {
+        // the x source (fp32 x or its planes) through xs / xb for a later copy
+        auto issue_weights = [&](int64_t j, const uint8_t *&xs, uint32_t &xb) {
             const int sl = (int)(j % C::S);
             uint8_t *base = ring + sl * L::SLOT_BYTES;
             const StreamProb &p = a.p[pi];
             const ChunkPos q = chunk_pos<FMT>(p, c);
             const int ng = (int)i64min(L::GPU, p.groups - gb * L::GPU);
             const uint32_t qbytes = q.nbc * C::VPB * kVecBytes;
-            xb = q.nbc * C::E * 4;
-            xs = p.x + (int64_t)(q.s * 8 + q.sub * C::BPC) * C::E;
+            const int64_t e0 = (int64_t)(q.s * 8 + q.sub * C::BPC) * C::E;  // first x element
+            if (planes) {
+                xb = q.nbc * (C::E / 32) * kXqBytes;
+                xs = a.xq + p.xq0 + (e0 / 32) * kXqBytes;
+            } else {
+                xb = q.nbc * C::E * 4;
+                xs = reinterpret_cast<const uint8_t *>(p.x + e0);
+            }
             mbar_arrive_expect_tx(&full[sl], ng * (qbytes + kVecBytes) + xb);
             const bool merged = q.sub * C::BPC + q.nbc == q.nblk;  // chunk ends at the scale vector
             for (int w = 0; w < ng; ++w) {
@@ -432,14 +594,18 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             }
             advance();
         };
-        auto issue_x = [&](int64_t j, const float *xs, uint32_t xb) {
+        auto issue_x = [&](int64_t j, const uint8_t *xs, uint32_t xb) {
             const int sl = (int)(j % C::S);
             bulk_g2s(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES, xs, xb, &full[sl]);
         };
         const int64_t nfill = i64min(C::S, nunits);
-        for (int64_t j = 0; j < nfill; ++j) issue_weights(j, xsrc[j], xbytes[j]);
-        pdl_wait();  // x may be written by the previous kernel on the stream
-        for (int64_t j = 0; j < nfill; ++j) issue_x(j, xsrc[j], xbytes[j]);
+#pragma unroll
+        for (int j = 0; j < C::S; ++j)
+            if (j < nfill) issue_weights(j, xsrc[j], xbytes[j]);
+        pdl_wait();  // x (or its planes) may be written by the previous kernel on the stream
+#pragma unroll
+        for (int j = 0; j < C::S; ++j)
+            if (j < nfill) issue_x(j, xsrc[j], xbytes[j]);
         for (int64_t j = nfill; j < nunits; ++j) {
             const int sl = (int)(j % C::S);
             if (*abort_flag || !mbar_wait(&empty[sl], (uint32_t)((j / C::S - 1) & 1), kWaitLimitNs)) {
@@ -449,7 +615,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
                     mbar_wait(&full[k % C::S], (uint32_t)((k / C::S) & 1), kWaitLimitNs);
                 return;
             }
-            const float *xs;
+            const uint8_t *xs;
             uint32_t xb;
             issue_weights(j, xs, xb);
             issue_x(j, xs, xb);
@@ -463,6 +629,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     // the CTA is stored; one shared with other CTAs (workspace mode) is
     // published and finished by the last CTA to arrive.
     const Magic mg = pin(a.mg);
+    const bool planes = XPlanes<FMT>::on && a.xq != nullptr;
     float acc[C::GPW];
 #pragma unroll
     for (int r = 0; r < C::GPW; ++r) acc[r] = 0.f;
@@ -483,7 +650,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             const uint8_t *ws = ring + sl * L::SLOT_BYTES + warp * L::CHUNK_BYTES;
             const float *xs =
                 reinterpret_cast<const float *>(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES);
-            consume_rows<FMT>(ws, xs, q.nbc, q.sub, nlive, lane, mg, acc);
+            consume_rows<FMT>(ws, xs, q.nbc, q.sub, nlive, lane, mg, planes, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sl]);  // the slot is free; the sums are in registers

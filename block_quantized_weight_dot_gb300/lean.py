@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "liblean_qmatmul.so")
 LEAN_Q4_0, LEAN_Q8_0, LEAN_I8_B64, LEAN_Q6_K = 0, 1, 2, 3
 LEAN_OK, LEAN_ERR_FORMAT, LEAN_ERR_SHAPE, LEAN_ERR_NULL, LEAN_ERR_ALIGN, LEAN_ERR_CUDA = range(6)
 LEAN_FLAG_EARLY_WEIGHTS = 1
+LEAN_FLAG_X_PLANES = 2
 
 # every symbol the header declares, with (restype, argtypes)
 _i64, _int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
@@ -166,7 +167,7 @@ def lean_qmatmul(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,
 
 def lean_qmatmul_ex(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,
                     flags: int = 0, stream=None) -> None:
-    """lean_qmatmul with launch flags (LEAN_FLAG_EARLY_WEIGHTS)."""
+    """lean_qmatmul with launch flags (LEAN_FLAG_EARLY_WEIGHTS, LEAN_FLAG_X_PLANES)."""
     _check("lean_qmatmul_ex", _lib.lean_qmatmul_ex(fmt, _addr(W_packed_dev), _addr(x_dev),
                                                    _addr(y_dev), N, K, M, flags, _stream(stream)))
 

@@ -141,7 +141,11 @@ enum {
      * of many small GEMVs needs.  Set it only when the preceding kernel on the
      * stream does not write W (weights uploaded by cudaMemcpy, or resident
      * model weights, are fine). */
-    LEAN_FLAG_EARLY_WEIGHTS = 1u
+    LEAN_FLAG_EARLY_WEIGHTS = 1u,
+    /* M = 1 with a workspace, Q4_0 / Q8_0 / I8_B64: always hand x to the
+     * product as integer planes (dp4a), not only when the call streams at
+     * least 32 MiB of weights.  Ignored otherwise. */
+    LEAN_FLAG_X_PLANES = 2u
 };
 
 /* lean_qmatmul with launch flags (LEAN_FLAG_*; unknown bits are rejected
@@ -168,7 +172,16 @@ int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);
  * larger than the SM count.
  *   workspace        device, 256-byte aligned, >= lean_qmatmul_workspace_bytes
  *                    bytes.  M = 1: it must be zeroed once (cudaMemset) before
- *                    its first use, and every call leaves it zeroed again.
+ *                    its first use; every call leaves its arrival counters
+ *                    zeroed again (the rest is scratch).  For Q4_0, Q8_0 and
+ *                    I8_B64 calls that stream at least 32 MiB of weights
+ *                    (lean_qmatmul_batch of a whole decode step, say), a
+ *                    first kernel also writes x there as integer
+ *                    planes (a power-of-two scale per 32 elements, 22 bits
+ *                    of the block's largest |x|) so that the dot products
+ *                    run on dp4a; results then differ from the fp32-x path
+ *                    by at most 2^-23 of each block's largest |x| times
+ *                    sum |w| per block.
  *                    M >= 16: any contents; a first kernel writes x there as
  *                    bf16 hi / lo operand tiles, once for all CTAs, which the
  *                    product then copies with TMA (the fast path for large M).

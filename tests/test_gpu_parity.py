@@ -201,8 +201,12 @@ def test_flags_rejected(lean):
     xd = torch.from_numpy(x).cuda()
     yd = torch.empty((1, N), device="cuda")
     st = torch.cuda.current_stream().cuda_stream
-    assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, 2,
+    assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, 4,
                                      st) == lean.LEAN_ERR_FORMAT
+    # the x-planes flag is known (and ignored without a workspace)
+    assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1,
+                                     lean.LEAN_FLAG_X_PLANES, st) == lean.LEAN_OK
+    torch.cuda.synchronize()
 
 
 # ---- workspace (stream-K split of row groups) and batched launches -------------
@@ -212,9 +216,11 @@ WS_SHAPES = [(1, 1), (33, 3), (64, 43), (100, 17), (32, 200), (65, 9)]
 
 @pytest.mark.parametrize("fmt", FMTS, ids=IDS)
 @pytest.mark.parametrize("N,nblk", WS_SHAPES)
-def test_workspace_split_groups(lean, fmt, N, nblk):
+@pytest.mark.parametrize("flags", [0, 2], ids=["fp32_x", "x_planes"])
+def test_workspace_split_groups(lean, fmt, N, nblk, flags):
     """M = 1 with a workspace: row groups split between CTAs are completed by
-    the last CTA; two calls in a row (the workspace must come back zeroed)."""
+    the last CTA; two calls in a row (the counters must come back zeroed);
+    x as fp32 or as integer planes (dp4a; Q6_K ignores the flag)."""
     torch = torch_cuda()
     be = syn.BLOCK_ELEMS[fmt]
     if fmt == syn.Q6_K:
@@ -230,20 +236,21 @@ def test_workspace_split_groups(lean, fmt, N, nblk):
     outs = []
     for _ in range(2):
         yd = torch.full((1, N), float("nan"), device="cuda")
-        lean.lean_qmatmul_ws(fmt, Wd, xd, yd, N, K, 1, 0, ws, nb)
+        lean.lean_qmatmul_ws(fmt, Wd, xd, yd, N, K, 1, flags, ws, nb)
         torch.cuda.synchronize()
         y = yd.cpu().numpy().astype(np.float64)
         check_close(y, y_ref, bound, "ws %s N=%d K=%d" % (syn.FORMAT_NAMES[fmt], N, K))
         outs.append(y)
     assert np.array_equal(outs[0], outs[1])
-    # the counters region must be back to zero
-    cnt_off = 512 * 2 * 8 * 32 * 4
-    assert int(ws[cnt_off:].count_nonzero()) == 0
+    # the arrival counters (the workspace's last 256-byte-rounded 4 * groups
+    # bytes) must be back to zero; the rest is scratch
+    cnt_bytes = (4 * ((N + 31) // 32) + 255) // 256 * 256
+    assert int(ws[nb - cnt_bytes:].count_nonzero()) == 0
     assert lean.lean_device_error(True) == 0
 
 
 @pytest.mark.parametrize("fmt", FMTS, ids=IDS)
-@pytest.mark.parametrize("use_ws", [False, True], ids=["whole_groups", "workspace"])
+@pytest.mark.parametrize("use_ws", [0, 1, 2], ids=["whole_groups", "workspace", "x_planes"])
 def test_batch(lean, fmt, use_ws):
     torch = torch_cuda()
     be = syn.BLOCK_ELEMS[fmt]
@@ -268,7 +275,8 @@ def test_batch(lean, fmt, use_ws):
     for rep in range(2):
         for it in items:
             it[2].fill_(float("nan"))
-        lean.lean_qmatmul_batch(fmt, probs, lean.LEAN_FLAG_EARLY_WEIGHTS, ws, nb)
+        flags = lean.LEAN_FLAG_EARLY_WEIGHTS | (lean.LEAN_FLAG_X_PLANES if use_ws == 2 else 0)
+        lean.lean_qmatmul_batch(fmt, probs, flags, ws, nb)
         torch.cuda.synchronize()
         for (Wd, xd, yd, N, K), (y_ref, bound) in zip(items, refs):
             check_close(yd.cpu().numpy().astype(np.float64)[None, :], y_ref, bound,

@@ -50,6 +50,41 @@ def test_decode_stack_layers():
         _full(lin)
 
 
+def test_decode_stack_batch_x_planes():
+    """The whole 32-layer decode step (224 GEMVs, 177 MB of Q4_0 weights) as
+    one lean_qmatmul_batch call with a workspace, the launch the benchmark
+    times: at this size x goes in as integer planes; every output of every
+    linear against the oracle."""
+    torch = torch_cuda()
+    from block_quantized_weight_dot_gb300 import lean
+    stack = syn.smollm2_360m_decode_stack()
+    items, keep, refs = [], [], []
+    for lin in stack.linears:
+        W, x = lin.make()
+        Wd = lean.upload_packed(lin.fmt, W, lin.N, lin.K)
+        xd = torch.from_numpy(np.ascontiguousarray(x.reshape(-1))).cuda()
+        yd = torch.full((lin.N,), float("nan"), device="cuda")
+        keep += [Wd, xd, yd]
+        items.append((Wd, xd, yd, lin.N, lin.K))
+        refs.append(oracle.qmatmul(lin.fmt, W, x, lin.N, lin.K, threads=THREADS))
+    probs = lean.make_problems(items)
+    nb = lean.lean_batch_workspace_bytes(syn.Q4_0, probs)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    outs = []
+    for rep in range(2):
+        for it in items:
+            it[2].fill_(float("nan"))
+        lean.lean_qmatmul_batch(syn.Q4_0, probs, lean.LEAN_FLAG_EARLY_WEIGHTS, ws, nb)
+        torch.cuda.synchronize()
+        ys = [it[2].cpu().numpy().astype(np.float64) for it in items]
+        for lin, y, (y_ref, bound) in zip(stack.linears, ys, refs):
+            check_close(y[None, :], y_ref, bound, "stack " + lin.name)
+        outs.append(ys)
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+    assert lean.lean_device_error(True) == 0
+
+
 @pytest.mark.parametrize("fmt", [syn.Q8_0, syn.I8_B64], ids=["q8_0", "i8_b64"])
 def test_tinyllama_full(fmt):
     torch_cuda()
