@@ -367,7 +367,8 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
                 xa.p[i].pad = 0;
             }
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)((max_nb + 7) / 8), (unsigned)n, 1);
+            cfg.gridDim = dim3((unsigned)((max_nb + 8 * kXprepBlocks - 1) / (8 * kXprepBlocks)),
+                               (unsigned)n, 1);
             cfg.blockDim = dim3(256, 1, 1);
             cfg.stream = stream;
             cudaLaunchAttribute attr[2];

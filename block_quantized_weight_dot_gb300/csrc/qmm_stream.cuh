@@ -103,7 +103,7 @@ template <int FMT> struct StreamCfg;
 #define LEAN_Q4_GPW 1
 #endif
 #ifndef LEAN_Q4_S
-#define LEAN_Q4_S 2
+#define LEAN_Q4_S 3
 #endif
 #ifndef LEAN_Q4_CPS
 #define LEAN_Q4_CPS 2
@@ -210,12 +210,11 @@ __device__ __forceinline__ int plane_pos(int l) {
     if (FMT == Q4_0) return 4 * (2 * (l >> 3) + (l & 1)) + ((l & 7) >> 1);
     return l;
 }
-// The warp converts one block of 32 elements of x (global) into its planes
-// at dst; lane l handles element l.
+// The warp converts one block of 32 elements of x into its planes at dst;
+// lane l holds element l in v.
 template <int FMT>
-__device__ __forceinline__ void x_block_to_planes(const float *xs, uint8_t *dst, int lane) {
+__device__ __forceinline__ void x_block_to_planes(float v, uint8_t *dst, int lane) {
     constexpr int OFF = FMT == Q4_0 ? 8 : 128;
-    const float v = xs[lane];
     const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
     // |x| * 2^s <= 2^22 for the block's largest |x| (s capped for tiny blocks)
     const int s = min(21 - ((int)(mx >> 23) - 127), 126);
@@ -236,8 +235,10 @@ __device__ __forceinline__ void x_block_to_planes(const float *xs, uint8_t *dst,
     }
 }
 
-// x of several problems as planes: blockIdx.y = problem, one warp per block
-// of 32 elements.  xq + p.xq0 receives the problem's K/32 plane blocks.
+// x of several problems as planes: blockIdx.y = problem, each warp converts
+// kXprepBlocks consecutive blocks of 32 elements (their loads issued first).
+// xq + p.xq0 receives the problem's K/32 plane blocks.
+constexpr int kXprepBlocks = 4;
 struct XprepProb {
     const float *x;
     int64_t xq0;
@@ -256,10 +257,17 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ Xpre
     pdl_launch_dependents();
     pdl_wait();  // x may come from the previous kernel on the stream
     const XprepProb &p = a.p[blockIdx.y];
-    const int b = (int)blockIdx.x * 8 + (int)(threadIdx.x >> 5);
-    if (b >= p.nb) return;
-    x_block_to_planes<FMT>(p.x + 32 * (int64_t)b, a.xq + p.xq0 + (int64_t)b * kXqBytes,
-                           (int)(threadIdx.x & 31));
+    const int lane = (int)(threadIdx.x & 31);
+    const int b0 = ((int)blockIdx.x * 8 + (int)(threadIdx.x >> 5)) * kXprepBlocks;
+    if (b0 >= p.nb) return;
+    float v[kXprepBlocks];
+#pragma unroll
+    for (int u = 0; u < kXprepBlocks; ++u)
+        v[u] = b0 + u < p.nb ? p.x[32 * (int64_t)(b0 + u) + lane] : 0.f;
+#pragma unroll
+    for (int u = 0; u < kXprepBlocks; ++u)
+        if (b0 + u < p.nb)
+            x_block_to_planes<FMT>(v[u], a.xq + p.xq0 + (int64_t)(b0 + u) * kXqBytes, lane);
 }
 
 __device__ __forceinline__ uint32_t dp4a_us(uint32_t a, uint32_t b, uint32_t c) {
