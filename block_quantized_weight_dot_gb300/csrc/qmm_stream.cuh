@@ -571,8 +571,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
         uint32_t xbytes[C::S];
         // arm slot j's barrier for the whole unit and copy the weights; returns
         // the x source (fp32 x or its planes) through xs / xb for a later copy
-        auto issue_weights = [&](int64_t j, const uint8_t *&xs, uint32_t &xb) {
-            const int sl = (int)(j % C::S);
+        auto issue_weights = [&](int sl, const uint8_t *&xs, uint32_t &xb) {
             uint8_t *base = ring + sl * L::SLOT_BYTES;
             const StreamProb &p = a.p[pi];
             const ChunkPos q = chunk_pos<FMT>(p, c);
@@ -602,8 +601,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             }
             advance();
         };
-        auto issue_x = [&](int64_t j, const uint8_t *xs, uint32_t xb) {
-            const int sl = (int)(j % C::S);
+        auto issue_x = [&](int sl, const uint8_t *xs, uint32_t xb) {
             bulk_g2s(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES, xs, xb, &full[sl]);
         };
         const int64_t nfill = i64min(C::S, nunits);
@@ -614,9 +612,13 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
 #pragma unroll
         for (int j = 0; j < C::S; ++j)
             if (j < nfill) issue_x(j, xsrc[j], xbytes[j]);
+        // slot and phase of unit j advance incrementally (no 64-bit division);
+        // unit j >= S waits for the consumers of unit j - S (the same slot, the
+        // previous phase)
+        int sl = (int)(nfill % C::S);
+        uint32_t ph = nfill == C::S ? 0u : 1u;  // phase parity of unit j - S on `empty`
         for (int64_t j = nfill; j < nunits; ++j) {
-            const int sl = (int)(j % C::S);
-            if (*abort_flag || !mbar_wait(&empty[sl], (uint32_t)((j / C::S - 1) & 1), kWaitLimitNs)) {
+            if (*abort_flag || !mbar_wait(&empty[sl], ph, kWaitLimitNs)) {
                 atomicOr(a.err, kErrEmptyTimeout);
                 // let the copies already issued land before the CTA can exit
                 for (int64_t k = i64max(0, j - C::S); k < j; ++k)
@@ -625,8 +627,12 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             }
             const uint8_t *xs;
             uint32_t xb;
-            issue_weights(j, xs, xb);
-            issue_x(j, xs, xb);
+            issue_weights(sl, xs, xb);
+            issue_x(sl, xs, xb);
+            if (++sl == C::S) {
+                sl = 0;
+                ph ^= 1u;
+            }
         }
         return;
     }
@@ -641,9 +647,10 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     float acc[C::GPW];
 #pragma unroll
     for (int r = 0; r < C::GPW; ++r) acc[r] = 0.f;
+    int sl = 0;
+    uint32_t ph = 0;  // phase parity of unit j on `full`
     for (int64_t j = 0; j < nunits; ++j) {
-        const int sl = (int)(j % C::S);
-        if (!mbar_wait(&full[sl], (uint32_t)((j / C::S) & 1), kWaitLimitNs)) {
+        if (!mbar_wait(&full[sl], ph, kWaitLimitNs)) {
             if (lane == 0) {
                 atomicOr(a.err, kErrFullTimeout);
                 *abort_flag = 1;
@@ -701,6 +708,10 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             for (int r = 0; r < C::GPW; ++r) acc[r] = 0.f;
         }
         advance();
+        if (++sl == C::S) {
+            sl = 0;
+            ph ^= 1u;
+        }
     }
 }
 
