@@ -294,12 +294,28 @@ inline bool stream_totals(const HostProb *ph, int n, int64_t *groups) {
     return true;
 }
 
+// Set the variant's shared-memory limit once per device and launch it.
+template <int FMT, int NP, bool PL>
+lean_status launch_stream_kernel(const StreamArgs<NP> &a, unsigned kflags, cudaStream_t stream) {
+    using L = StreamLayout<FMT, PL>;
+    static std::atomic<uint64_t> smem_done{0};
+    auto kern = qmm_stream_kernel<FMT, NP, PL>;
+    if (!ensure_smem(kern, L::SMEM, smem_done)) return LEAN_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.ctas, 1, 1);
+    cfg.blockDim = dim3(kStreamThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    fill_launch(cfg, attr, 1, kflags);
+    return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
+}
+
 template <int FMT, int NP>
 lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
                           bool planes, unsigned *err, cudaStream_t stream) {
     using C = StreamCfg<FMT>;
-    using L = StreamLayout<FMT>;
-    static std::atomic<uint64_t> smem_done{0};
+    using L = StreamLayout<FMT>;  // the ring geometry that both variants share
     StreamArgs<NP> a;
     a.nprob = n;
     a.pad = 0;
@@ -332,8 +348,8 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
     a.mg = make_magic();
     a.err = err;
     a.xq = nullptr;
-    const int64_t slots = std::min<int64_t>((int64_t)sm_count() * C::CPS, kMaxStreamCtas);
     unsigned kflags = flags;
+    bool use_planes = false;
     if (ws != nullptr) {
         // room for the x planes of every problem, back to back (the layout is
         // the one lean_*_workspace_bytes describe, planes used or not)
@@ -347,10 +363,11 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
                 max_nb = std::max<int>(max_nb, (int)(ph[i].g.K / 32));
             }
         }
-        const bool use_planes =
-            xqb > 0 && (wbytes >= kPlanesMinWeightBytes || (flags & LEAN_FLAG_X_PLANES));
+        use_planes = xqb > 0 && (wbytes >= kPlanesMinWeightBytes || (flags & LEAN_FLAG_X_PLANES));
         const WorkspaceLayout wl = workspace_layout(groups, xqb);
         if (ws_bytes < wl.total) return LEAN_ERR_SHAPE;
+        const int cps = use_planes ? StreamRing<FMT, true>::CPS : StreamRing<FMT, false>::CPS;
+        const int64_t slots = std::min<int64_t>((int64_t)sm_count() * cps, kMaxStreamCtas);
         a.balanced = 1;
         a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, units));
         a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + wl.part_off);
@@ -381,21 +398,15 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
             kflags = LEAN_FLAG_EARLY_WEIGHTS;
         }
     } else {
+        const int64_t slots =
+            std::min<int64_t>((int64_t)sm_count() * StreamRing<FMT, false>::CPS, kMaxStreamCtas);
         a.balanced = 0;
         a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, gblocks));
         a.part = nullptr;
         a.cnt = nullptr;
     }
-    auto kern = qmm_stream_kernel<FMT, NP>;
-    if (!ensure_smem(kern, L::SMEM, smem_done)) return LEAN_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.ctas, 1, 1);
-    cfg.blockDim = dim3(kStreamThreads, 1, 1);
-    cfg.dynamicSmemBytes = L::SMEM;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    fill_launch(cfg, attr, 1, kflags);
-    return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
+    if (use_planes) return launch_stream_kernel<FMT, NP, true>(a, kflags, stream);
+    return launch_stream_kernel<FMT, NP, false>(a, kflags, stream);
 }
 
 template <int FMT>

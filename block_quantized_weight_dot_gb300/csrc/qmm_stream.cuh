@@ -116,6 +116,23 @@ template <> struct StreamCfg<Q8_0> { static constexpr int VPB = 2, BPC = 4, E = 
 template <> struct StreamCfg<I8_B64> { static constexpr int VPB = 4, BPC = 2, E = 64, S = 2, CPS = 2, GPW = 1; };
 template <> struct StreamCfg<Q6_K> { static constexpr int VPB = 13, BPC = 1, E = 256, S = 3, CPS = 1, GPW = 1; };
 
+// Ring depth and CTAs per SM of a kernel variant (PL: x as planes, dp4a; that
+// variant needs no decode constants in registers, so more CTAs may fit).
+#ifndef LEAN_Q4P_S
+#define LEAN_Q4P_S 3
+#endif
+#ifndef LEAN_Q4P_CPS
+#define LEAN_Q4P_CPS 2
+#endif
+template <int FMT, bool PL>
+struct StreamRing {
+    static constexpr int S = StreamCfg<FMT>::S, CPS = StreamCfg<FMT>::CPS;
+};
+template <>
+struct StreamRing<Q4_0, true> {
+    static constexpr int S = LEAN_Q4P_S, CPS = LEAN_Q4P_CPS;
+};
+
 // x as integer planes (dp4a) for the integer formats
 template <int FMT> struct XPlanes { static constexpr bool on = FMT != Q6_K; };
 // One 32-element block of x in plane form: {init2, init1, init0, 2^-s} then
@@ -123,9 +140,10 @@ template <int FMT> struct XPlanes { static constexpr bool on = FMT != Q6_K; };
 constexpr int kXqBytes = kXqBlockBytes;
 static_assert(kXqBytes == 16 + 3 * 32, "header + three planes");
 
-template <int FMT>
+template <int FMT, bool PL = false>
 struct StreamLayout {
     using C = StreamCfg<FMT>;
+    static constexpr int S = StreamRing<FMT, PL>::S;
     static constexpr int CPSTEP = 8 / C::BPC;                          // chunks of a full step
     static constexpr int CHUNK_BYTES = (C::BPC * C::VPB + 1) * kVecBytes;  // one group's chunk
     static constexpr int XE = C::BPC * C::E;                           // x elements of a unit
@@ -133,10 +151,10 @@ struct StreamLayout {
     static constexpr int SLOT_BYTES = GPU * CHUNK_BYTES + XE * 4;  // planes take less than fp32
     // shared memory: [full S][empty S][abort][pad][ring S*SLOT]
     static constexpr int OFF_FULL = 0;
-    static constexpr int OFF_EMPTY = 8 * C::S;
-    static constexpr int OFF_ABORT = 16 * C::S;
+    static constexpr int OFF_EMPTY = 8 * S;
+    static constexpr int OFF_ABORT = 16 * S;
     static constexpr int OFF_RING = 128;
-    static constexpr int SMEM = OFF_RING + C::S * SLOT_BYTES;
+    static constexpr int SMEM = OFF_RING + S * SLOT_BYTES;
     static_assert(OFF_ABORT + 4 <= OFF_RING, "barriers fit before the ring");
 };
 
@@ -513,11 +531,12 @@ __device__ __forceinline__ void consume_rows(const uint8_t *ws, const float *xs,
         if (r < nlive) acc[r] += consume_chunk<FMT>(ws + r * stride, xs, nbc, sub, lane, mg, planes);
 }
 
-template <int FMT, int NP>
-__global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
+template <int FMT, int NP, bool PL>
+__global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
     qmm_stream_kernel(const __grid_constant__ StreamArgs<NP> a) {
     using C = StreamCfg<FMT>;
-    using L = StreamLayout<FMT>;
+    using L = StreamLayout<FMT, PL>;
+    constexpr int S = L::S;
     constexpr int SV = 8 * C::VPB + 1;  // vectors of a full step
     extern __shared__ __align__(128) uint8_t sbuf[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sbuf + L::OFF_FULL);
@@ -534,7 +553,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::S; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kStreamWarps);
         }
@@ -566,9 +585,9 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     if (warp == kStreamWarps) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        const bool planes = XPlanes<FMT>::on && a.xq != nullptr;
-        const uint8_t *xsrc[C::S];
-        uint32_t xbytes[C::S];
+        constexpr bool planes = PL && XPlanes<FMT>::on;
+        const uint8_t *xsrc[S];
+        uint32_t xbytes[S];
         // arm slot j's barrier for the whole unit and copy the weights; returns
         // the x source (fp32 x or its planes) through xs / xb for a later copy
         auto issue_weights = [&](int sl, const uint8_t *&xs, uint32_t &xb) {
@@ -604,32 +623,32 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
         auto issue_x = [&](int sl, const uint8_t *xs, uint32_t xb) {
             bulk_g2s(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES, xs, xb, &full[sl]);
         };
-        const int64_t nfill = i64min(C::S, nunits);
+        const int64_t nfill = i64min(S, nunits);
 #pragma unroll
-        for (int j = 0; j < C::S; ++j)
+        for (int j = 0; j < S; ++j)
             if (j < nfill) issue_weights(j, xsrc[j], xbytes[j]);
         pdl_wait();  // x (or its planes) may be written by the previous kernel on the stream
 #pragma unroll
-        for (int j = 0; j < C::S; ++j)
+        for (int j = 0; j < S; ++j)
             if (j < nfill) issue_x(j, xsrc[j], xbytes[j]);
         // slot and phase of unit j advance incrementally (no 64-bit division);
         // unit j >= S waits for the consumers of unit j - S (the same slot, the
         // previous phase)
-        int sl = (int)(nfill % C::S);
-        uint32_t ph = nfill == C::S ? 0u : 1u;  // phase parity of unit j - S on `empty`
+        int sl = (int)(nfill % S);
+        uint32_t ph = nfill == S ? 0u : 1u;  // phase parity of unit j - S on `empty`
         for (int64_t j = nfill; j < nunits; ++j) {
             if (*abort_flag || !mbar_wait(&empty[sl], ph, kWaitLimitNs)) {
                 atomicOr(a.err, kErrEmptyTimeout);
                 // let the copies already issued land before the CTA can exit
-                for (int64_t k = i64max(0, j - C::S); k < j; ++k)
-                    mbar_wait(&full[k % C::S], (uint32_t)((k / C::S) & 1), kWaitLimitNs);
+                for (int64_t k = i64max(0, j - S); k < j; ++k)
+                    mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), kWaitLimitNs);
                 return;
             }
             const uint8_t *xs;
             uint32_t xb;
             issue_weights(sl, xs, xb);
             issue_x(sl, xs, xb);
-            if (++sl == C::S) {
+            if (++sl == S) {
                 sl = 0;
                 ph ^= 1u;
             }
@@ -642,8 +661,9 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
     // registers until a group's last chunk in this CTA.  A group complete in
     // the CTA is stored; one shared with other CTAs (workspace mode) is
     // published and finished by the last CTA to arrive.
-    const Magic mg = pin(a.mg);
-    const bool planes = XPlanes<FMT>::on && a.xq != nullptr;
+    constexpr bool planes = PL && XPlanes<FMT>::on;
+    Magic mg;  // decode constants, in registers only for the fp32-x variant
+    if constexpr (!planes) mg = pin(a.mg);
     float acc[C::GPW];
 #pragma unroll
     for (int r = 0; r < C::GPW; ++r) acc[r] = 0.f;
@@ -708,7 +728,7 @@ __global__ void __launch_bounds__(kStreamThreads, StreamCfg<FMT>::CPS)
             for (int r = 0; r < C::GPW; ++r) acc[r] = 0.f;
         }
         advance();
-        if (++sl == C::S) {
+        if (++sl == S) {
             sl = 0;
             ph ^= 1u;
         }
