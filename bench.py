@@ -43,6 +43,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise MAX of per-rank timings over the initialised process group
+    (the job's step time is its slowest rank's); the values unchanged on one
+    rank or without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_gbs(bytes_per_step_per_rank, ms_per_step, world):
+    """Whole-job throughput of `world` replicas that each process one step of
+    `bytes_per_step_per_rank` in `ms_per_step` (weak scaling)."""
+    return bytes_per_step_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -330,9 +349,7 @@ def time_gpu(args, wl):
 
     if ws > 1:
         import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+        ms, e2e_ms = max_over_ranks([ms, e2e_ms], device)
         dist.destroy_process_group()
     kernel = ("qmm_stream_kernel<%s,%s> (TMA ring, %s)"
               % (syn.FORMAT_NAMES[dw.lins[0].fmt], "batch" if dw.batch is not None else "1",
@@ -426,7 +443,7 @@ def main():
     if rank != 0:
         return
     s_step = r["ms"] * 1e-3
-    gbs = alg_bytes / s_step / 1e9 * ws
+    gbs = job_gbs(alg_bytes, r["ms"], ws)
     linears_per_s = n_lin / s_step * ws
     # the stream kernel moves every algorithmic byte of the step; its duration
     # is taken as the whole step (with the x-plane kernel, which only reads x,
@@ -458,7 +475,7 @@ def main():
                      "duration": "whole step (all launches of the step), a lower bound for "
                                  "the stream kernel alone"},
         "cpu_baseline": cpu,
-        "e2e": {"value": alg_bytes / (r["e2e_ms"] * 1e-3) / 1e9 * ws, "unit": "GB/s",
+        "e2e": {"value": job_gbs(alg_bytes, r["e2e_ms"], ws), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "ms_per_step": r["e2e_ms"]},
         "gpu_launches": r["launches"] * args.steps,
