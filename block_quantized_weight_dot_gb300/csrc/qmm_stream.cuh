@@ -308,13 +308,21 @@ __device__ __forceinline__ float plane_dot(const uint32_t (&w)[8], const uint8_t
     const uint32_t P2[8] = {a2.x, a2.y, a2.z, a2.w, b2.x, b2.y, b2.z, b2.w};
     const uint32_t P1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
     const uint32_t P0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
+    // two independent chains per plane (even and odd words) for latency
     uint32_t s2 = (uint32_t)h.x, s1 = (uint32_t)h.y, s0 = (uint32_t)h.z;
+    uint32_t t2 = 0, t1 = 0, t0 = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 8; i += 2) {
         s2 = dp4a_us(w[i], P2[i], s2);
         s1 = dp4a_uu(w[i], P1[i], s1);
         s0 = dp4a_uu(w[i], P0[i], s0);
+        t2 = dp4a_us(w[i + 1], P2[i + 1], t2);
+        t1 = dp4a_uu(w[i + 1], P1[i + 1], t1);
+        t0 = dp4a_uu(w[i + 1], P0[i + 1], t0);
     }
+    s2 += t2;
+    s1 += t1;
+    s0 += t0;
     const float T = fmaf((float)(int)s2, 65536.f, fmaf((float)(int)s1, 256.f, (float)(int)s0));
     return __int_as_float(h.w) * T;
 }
