@@ -17,6 +17,22 @@ using namespace lean;
 __device__ unsigned lean_error_word;
 
 namespace {
+constexpr unsigned kErrSelftest = 8u;
+
+// One block waits on an mbarrier that nothing completes, for limit_ns.
+__global__ void wait_selftest_kernel(unsigned *err, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool done = mbar_wait(&bar, 0u, limit_ns);
+    if (__syncthreads_or(!done) && threadIdx.x == 0) atomicOr(err, kErrSelftest);
+}
+}  // namespace
+
+namespace {
 
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
@@ -188,6 +204,15 @@ lean_status lean_dequant(int fmt, const void *W_packed_dev, float *w_dev, int64_
     case LEAN_Q6_K: return dequant_fmt<Q6_K>(g, W, w_dev, s);
     }
     return LEAN_ERR_FORMAT;
+}
+
+lean_status lean_wait_selftest(unsigned limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 1000000) return LEAN_ERR_SHAPE;
+    unsigned *err = error_word();
+    if (!err) return LEAN_ERR_CUDA;
+    cudaGetLastError();
+    wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err, (uint64_t)limit_us * 1000u);
+    return cudaGetLastError() == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
 }
 
 unsigned lean_device_error(int clear) {

@@ -40,6 +40,7 @@ SIGNATURES = {
     "lean_batch_workspace_bytes": (_i64, [_int, _int, _vp]),
     "lean_qmatmul_batch": (_int, [_int, _int, _vp, ctypes.c_uint, _vp, _i64, _vp]),
     "lean_device_error": (ctypes.c_uint, [_int]),
+    "lean_wait_selftest": (_int, [ctypes.c_uint, _vp]),
     "lean_qmatmul_fixed_ws": (_int, [_int, _vp, _vp, _vp, _i64, _i64, ctypes.c_uint, _vp]),
     "lean_fixed_workspace_bytes": (_i64, []),
     "lean_status_str": (ctypes.c_char_p, [_int]),
@@ -228,6 +229,12 @@ def lean_fixed_workspace_bytes() -> int:
 def lean_device_error(clear: bool = True) -> int:
     """Device error word (non-zero: a kernel's bounded wait timed out)."""
     return _lib.lean_device_error(1 if clear else 0)
+
+
+def lean_wait_selftest(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test: a block waits on a barrier nothing
+    completes, gives up after limit_us and sets bit 8 of the error word."""
+    _check("lean_wait_selftest", _lib.lean_wait_selftest(limit_us, _stream(stream)))
 
 
 # ---- torch conveniences (device memory via PyTorch; compute via the library) ----

@@ -242,10 +242,19 @@ int64_t lean_fixed_workspace_bytes(void);
 
 /* The device error word of the current device: non-zero when a kernel gave up
  * waiting on one of its own pipeline barriers (a bounded wait timed out and
- * the kernel returned early; its outputs are then invalid).  Reads it
+ * the kernel returned early; its outputs are then invalid).  Bits: 1 a stream
+ * consumer waited too long for a slot, 2 a stream producer for a free slot,
+ * 4 the tensor-core product for a stage, 8 lean_wait_selftest.  Reads it
  * synchronously (the device is synchronised first) and clears it when
  * `clear` is non-zero.  Returns 0xFFFFFFFF if the word cannot be read. */
 unsigned lean_device_error(int clear);
+
+/* Self-test of the bounded waits: launches one 32-thread block on `stream`
+ * that waits, with the same bounded mbarrier wait the kernels use, on a
+ * barrier that nothing completes, gives up after `limit_us` microseconds
+ * (1 .. 1000000) and sets bit 8 of the device error word.  The context stays
+ * usable.  LEAN_ERR_SHAPE for a limit out of range. */
+lean_status lean_wait_selftest(unsigned limit_us, void *stream);
 
 /* Static description of a status code. */
 const char *lean_status_str(int status);

@@ -305,3 +305,32 @@ def test_batch_argument_errors(lean):
     assert f(0, 1, p, 0, ws.data_ptr(), 64, st) == lean.LEAN_ERR_SHAPE  # too small
     assert f(0, 1, p, 0, None, 0, st) == lean.LEAN_OK
     torch.cuda.synchronize()
+
+
+def test_bounded_wait_times_out(lean):
+    """A bounded wait on a barrier that nothing completes gives up, sets its bit
+    of the device error word and leaves the context usable."""
+    import time
+    torch = torch_cuda()
+    assert lean.lean_device_error(True) == 0
+    assert lean._lib.lean_wait_selftest(0, None) == lean.LEAN_ERR_SHAPE
+    assert lean._lib.lean_wait_selftest(1000001, None) == lean.LEAN_ERR_SHAPE
+    t0 = time.perf_counter()
+    lean.lean_wait_selftest(20000)  # 20 ms
+    torch.cuda.synchronize()
+    took = time.perf_counter() - t0
+    assert 0.015 < took < 2.0, took
+    assert lean.lean_device_error(False) == 8
+    assert lean.lean_device_error(True) == 8
+    assert lean.lean_device_error(True) == 0
+    # the context still runs products
+    fmt, N, K = syn.Q4_0, 96, 256
+    W, x = syn.make_problem(fmt, N, K, 1, seed=(32,))
+    Wd = lean.upload_packed(fmt, W, N, K)
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.full((1, N), float("nan"), device="cuda")
+    lean.lean_qmatmul(fmt, Wd, xd, yd, N, K, 1)
+    torch.cuda.synchronize()
+    y_ref, bound = oracle.qmatmul(fmt, W, x, N, K)
+    check_close(yd.cpu().numpy().astype(np.float64), y_ref, bound, "after self-test")
+    assert lean.lean_device_error(True) == 0
