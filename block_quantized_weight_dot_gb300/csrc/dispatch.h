@@ -26,16 +26,19 @@ struct HostProb {
 
 // Workspace of the balanced (stream-K) GEMV: per-CTA partial sums of the row
 // groups split between CTAs (two sides x 16 groups x 32 rows), then x as
-// integer planes (xq_bytes, may be 0), then one arrival counter per row group.
+// integer planes (xq_bytes, may be 0), then one arrival counter per row group
+// and, for a batch (handout), the two counters of the run-time hand-out of
+// group blocks.
 struct WorkspaceLayout {
     int64_t part_off, xq_off, cnt_off, total;
 };
-inline WorkspaceLayout workspace_layout(int64_t groups, int64_t xq_bytes = 0) {
+inline WorkspaceLayout workspace_layout(int64_t groups, int64_t xq_bytes = 0,
+                                        bool handout = false) {
     WorkspaceLayout w;
     w.part_off = 0;
     w.xq_off = (int64_t)kMaxStreamCtas * 2 * 16 * 32 * 4;
     w.cnt_off = w.xq_off + (xq_bytes + 255) / 256 * 256;
-    w.total = w.cnt_off + (groups * 4 + 255) / 256 * 256;
+    w.total = w.cnt_off + ((groups + (handout ? 2 : 0)) * 4 + 255) / 256 * 256;
     return w;
 }
 // x planes pay for their extra launch only when the call streams this many

@@ -311,6 +311,55 @@ lean_status launch_stream_kernel(const StreamArgs<NP> &a, unsigned kflags, cudaS
     return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
 }
 
+// Run-time hand-out of whole group blocks: worth it when a batch has many more
+// group blocks than CTAs, so that the last blocks taken are short.
+constexpr int64_t kDynMinBlocksPerCta = 3;
+// On the decode step one unit costs its consumer warps about as long as
+// streaming this many bytes, on top of its own bytes (measured: the finish
+// time of a CTA grew by ~0.7 us per unit and ~0.026 us per KB).
+constexpr int64_t kUnitFixedBytes = 27 * 1024;
+
+// Runs of group blocks in hand-out order, largest blocks first: for each
+// problem its full group blocks (one run) and its last, partial block (a run of
+// one), sorted by the cost of one block (bytes copied plus a fixed cost per
+// unit); ties keep problem order.
+template <int FMT, bool PL, int NP>
+void dyn_runs(StreamArgs<NP> &a) {
+    using C = StreamCfg<FMT>;
+    using L = StreamLayout<FMT, PL>;
+    auto unit_bytes = [](int64_t ng, int nbc) -> int64_t {
+        const int64_t xb = (PL && XPlanes<FMT>::on) ? (int64_t)nbc * (C::E / 32) * kXqBytes
+                                                    : (int64_t)nbc * C::E * 4;
+        return ng * ((int64_t)nbc * C::VPB + 1) * kVecBytes + xb;
+    };
+    struct Run {
+        int32_t code;
+        int64_t count, cost;
+    };
+    Run runs[2 * NP];
+    int nr = 0;
+    for (int i = 0; i < a.nprob; ++i) {
+        const StreamProb &p = a.p[i];
+        const int last_nbc = p.last_blocks - ((p.last_blocks + C::BPC - 1) / C::BPC - 1) * C::BPC;
+        auto block_cost = [&](int64_t ng) {
+            return (p.chunks - 1) * unit_bytes(ng, C::BPC) + unit_bytes(ng, last_nbc) +
+                   p.chunks * kUnitFixedBytes;
+        };
+        const int64_t full = p.groups / L::GPU, part = p.groups % L::GPU;
+        if (full > 0) runs[nr++] = Run{i, full, block_cost(L::GPU)};
+        if (part > 0) runs[nr++] = Run{i | (1 << 16), 1, block_cost(part)};
+    }
+    std::stable_sort(runs, runs + nr, [](const Run &x, const Run &y) { return x.cost > y.cost; });
+    int64_t item = 0;
+    for (int r = 0; r < nr; ++r) {
+        a.run_prob[r] = runs[r].code;
+        a.run_item0[r] = (int32_t)item;
+        item += runs[r].count;
+    }
+    a.run_item0[nr] = (int32_t)item;
+    a.nruns = nr;
+}
+
 template <int FMT, int NP>
 lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
                           bool planes, unsigned *err, cudaStream_t stream) {
@@ -348,6 +397,9 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
     a.mg = make_magic();
     a.err = err;
     a.xq = nullptr;
+    a.dyn = nullptr;
+    a.nruns = 0;
+    a.pad2 = 0;
     unsigned kflags = flags;
     bool use_planes = false;
     if (ws != nullptr) {
@@ -364,7 +416,7 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
             }
         }
         use_planes = xqb > 0 && (wbytes >= kPlanesMinWeightBytes || (flags & LEAN_FLAG_X_PLANES));
-        const WorkspaceLayout wl = workspace_layout(groups, xqb);
+        const WorkspaceLayout wl = workspace_layout(groups, xqb, n > 1);
         if (ws_bytes < wl.total) return LEAN_ERR_SHAPE;
         const int cps = use_planes ? StreamRing<FMT, true>::CPS : StreamRing<FMT, false>::CPS;
         const int64_t slots = std::min<int64_t>((int64_t)sm_count() * cps, kMaxStreamCtas);
@@ -372,6 +424,13 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
         a.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, units));
         a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + wl.part_off);
         a.cnt = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + wl.cnt_off);
+        if (n > 1 && gblocks >= kDynMinBlocksPerCta * slots && gblocks <= INT32_MAX &&
+            a.nprob <= 0xFFFF) {
+            a.balanced = 3;
+            a.ctas = (int)slots;
+            a.dyn = a.cnt + groups;
+            if (use_planes) dyn_runs<FMT, true>(a); else dyn_runs<FMT, false>(a);
+        }
         if (use_planes) {
             XprepArgs<NP> xa;
             xa.nprob = n;

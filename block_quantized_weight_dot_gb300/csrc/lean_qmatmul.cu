@@ -164,7 +164,7 @@ int64_t lean_batch_workspace_bytes(int fmt, int count, const lean_problem *probl
         groups += g.groups;
         xqb += xq_bytes(fmt, problems[i].K);
     }
-    return workspace_layout(groups, xqb).total;
+    return workspace_layout(groups, xqb, count > 1).total;
 }
 
 lean_status lean_qmatmul_batch(int fmt, int count, const lean_problem *problems, unsigned flags,

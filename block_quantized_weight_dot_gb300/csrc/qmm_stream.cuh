@@ -32,6 +32,13 @@
 //    blocks; with one they hold equal numbers of units (stream-K) and a group
 //    split between CTAs is completed by the last CTA to arrive, which adds the
 //    parts in CTA order: results are deterministic either way;
+//  - a batch with many more group blocks than CTAs (a whole decode step) is
+//    instead handed out at run time, one whole group block at a time, largest
+//    blocks first, from a counter in the workspace: CTAs that run faster
+//    take more blocks, so they all finish within about one block of each
+//    other (static ranges left the slowest SM several microseconds behind).
+//    A group block never splits, so each row is still summed in one fixed
+//    order;
 //  - weights are requested before griddepcontrol.wait and x after it, so with
 //    programmatic dependent launch the weight stream of one product overlaps
 //    the tail of the previous kernel on the stream;
@@ -80,16 +87,27 @@ template <int NP>
 struct StreamArgs {
     int nprob;
     int ctas;
-    int balanced;  // 1: equal units per CTA (needs part/cnt); 0: whole group blocks
+    int balanced;  // 1: equal units per CTA (needs part/cnt); 0: whole group blocks;
+                   // 3: whole group blocks taken at run time (needs dyn)
     int pad;
     int64_t total_units, total_gblocks;
     float *part;    // [ctas][2][8][32] partial sums of groups split between CTAs
     unsigned *cnt;  // [total groups] arrival counters, all zero between calls
     unsigned *err;  // device error word (bits of StreamError)
     const uint8_t *xq;  // x as planes (xprep_kernel), or null: fp32 x
+    unsigned *dyn;      // balanced == 3: [0] blocks taken after the first one of
+                        // each CTA, [1] CTAs done taking; both zero between calls
+    int nruns;          // balanced == 3: runs of group blocks, largest blocks first
+    int pad2;
     Magic mg;
     StreamProb p[NP];
+    // run r: problem run_prob[r] & 0xFFFF, its full group blocks (bit 16 clear)
+    // or its last, partial one (set); its blocks are items run_item0[r] ..
+    // run_item0[r + 1] - 1 of the hand-out order
+    int32_t run_prob[2 * NP];
+    int32_t run_item0[2 * NP + 1];
 };
+static_assert(sizeof(StreamArgs<256>) <= 32764, "kernel parameters fit the launch limit");
 
 template <int FMT> struct StreamCfg;
 // VPB: quant vectors per block; BPC: blocks per chunk; E: weights per block;
@@ -149,13 +167,14 @@ struct StreamLayout {
     static constexpr int XE = C::BPC * C::E;                           // x elements of a unit
     static constexpr int GPU = kStreamWarps * C::GPW;                  // row groups of a unit
     static constexpr int SLOT_BYTES = GPU * CHUNK_BYTES + XE * 4;  // planes take less than fp32
-    // shared memory: [full S][empty S][abort][pad][ring S*SLOT]
+    // shared memory: [full S][empty S][abort][info S][ring S*SLOT]; info:
+    // which unit a slot holds when units are taken at run time
     static constexpr int OFF_FULL = 0;
     static constexpr int OFF_EMPTY = 8 * S;
     static constexpr int OFF_ABORT = 16 * S;
-    static constexpr int OFF_RING = 128;
+    static constexpr int OFF_INFO = (OFF_ABORT + 4 + 15) / 16 * 16;
+    static constexpr int OFF_RING = (OFF_INFO + 16 * S + 127) / 128 * 128;
     static constexpr int SMEM = OFF_RING + S * SLOT_BYTES;
-    static_assert(OFF_ABORT + 4 <= OFF_RING, "barriers fit before the ring");
 };
 
 __device__ __forceinline__ int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -199,6 +218,26 @@ __device__ __forceinline__ int64_t cta_of_unit(const StreamArgs<NP> &a, int64_t 
     while (i > 0 && a.total_units * i / a.ctas > u) --i;
     return i;
 }
+
+// Problem and group block of item k of the run-time hand-out order.
+template <int NP>
+__device__ __forceinline__ void item_gblock(const StreamArgs<NP> &a, int64_t k, int &pi,
+                                            int64_t &gb) {
+    int lo = 0, hi = a.nruns - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.run_item0[mid] <= k) lo = mid; else hi = mid - 1;
+    }
+    const int r = a.run_prob[lo];
+    pi = r & 0xFFFF;
+    gb = (r >> 16) ? a.p[pi].gblocks - 1 : k - a.run_item0[lo];
+}
+// the unit a slot holds (run-time hand-out); pi < 0: no more units
+struct SlotInfo {
+    int pi;
+    int c;
+    int64_t gb;
+};
 
 // Where a unit's chunk sits in its groups' streams.
 struct ChunkPos {
@@ -550,11 +589,13 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
     uint64_t *full = reinterpret_cast<uint64_t *>(sbuf + L::OFF_FULL);
     uint64_t *empty = reinterpret_cast<uint64_t *>(sbuf + L::OFF_EMPTY);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbuf + L::OFF_ABORT);
+    SlotInfo *info = reinterpret_cast<SlotInfo *>(sbuf + L::OFF_INFO);
     uint8_t *ring = sbuf + L::OFF_RING;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t cta = blockIdx.x;
-    const int64_t beg = range_begin(a, cta), end = range_begin(a, cta + 1);
+    const bool dyn = a.balanced == 3;  // whole group blocks taken at run time
+    const int64_t beg = dyn ? 0 : range_begin(a, cta), end = dyn ? 0 : range_begin(a, cta + 1);
     const int64_t nunits = end - beg;
 
     // Let the next kernel on the stream start streaming its own weights.
@@ -569,13 +610,18 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
         fence_mbar_init();
     }
     __syncthreads();
-    if (nunits <= 0) return;
+    if (!dyn && nunits <= 0) return;
 
-    // cursor over the CTA's units: problem, group block inside it, chunk
-    int pi = find_prob_by_unit(a, beg);
+    // cursor over the CTA's units: problem, group block inside it, chunk (with
+    // run-time hand-out: the CTA's first group block is item blockIdx.x)
+    int pi;
     int64_t gb;
     int c;
-    {
+    if (dyn) {
+        item_gblock(a, cta, pi, gb);
+        c = 0;
+    } else {
+        pi = find_prob_by_unit(a, beg);
         const int64_t o = beg - a.p[pi].unit0;
         gb = o / a.p[pi].chunks;
         c = (int)(o % a.p[pi].chunks);
@@ -583,7 +629,7 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
     auto advance = [&]() {
         if (++c == a.p[pi].chunks) {
             c = 0;
-            if (++gb == a.p[pi].gblocks) {
+            if (!dyn && ++gb == a.p[pi].gblocks) {
                 gb = 0;
                 ++pi;
             }
@@ -631,6 +677,69 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
         auto issue_x = [&](int sl, const uint8_t *xs, uint32_t xb) {
             bulk_g2s(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES, xs, xb, &full[sl]);
         };
+        // after a timeout: let the copies already issued (units j - S .. j - 1)
+        // land before the CTA can exit
+        auto drain = [&](int64_t j) {
+            for (int64_t k = i64max(0, j - S); k < j; ++k)
+                mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), kWaitLimitNs);
+        };
+        if (dyn) {
+            // Units of the CTA's first group block go out before griddepcontrol.wait
+            // (weights only, at most S of them); the counter is read after it,
+            // once the previous kernel on the stream has finished with it.
+            bool waited = false;
+            int ndef = 0;  // x copies held back until the wait (slots 0 .. ndef - 1)
+            auto wait_prev = [&]() {
+                pdl_wait();
+                waited = true;
+                for (int k = 0; k < ndef; ++k) issue_x(k, xsrc[k], xbytes[k]);
+            };
+            // unit j >= S waits for the consumers of unit j - S (same slot)
+            auto slot_free = [&](int64_t j) {
+                return j < S || (!*abort_flag &&
+                                 mbar_wait(&empty[j % S], (uint32_t)((j / S - 1) & 1), kWaitLimitNs));
+            };
+            int64_t j = 0;
+            while (pi >= 0) {
+                if (!slot_free(j)) {
+                    atomicOr(a.err, kErrEmptyTimeout);
+                    drain(j);
+                    return;
+                }
+                const int sl = (int)(j % S);
+                info[sl] = SlotInfo{pi, c, gb};
+                const uint8_t *xs;
+                uint32_t xb;
+                issue_weights(sl, xs, xb);  // moves c on; c == 0: the block is done
+                if (waited) {
+                    issue_x(sl, xs, xb);
+                } else {
+                    xsrc[ndef] = xs;
+                    xbytes[ndef] = xb;
+                    ++ndef;
+                }
+                ++j;
+                if (!waited && (j == S || c == 0)) wait_prev();
+                if (c == 0) {  // take the next group block
+                    const int64_t k = (int64_t)atomicAdd(&a.dyn[0], 1u) + a.ctas;
+                    if (k < a.total_gblocks) item_gblock(a, k, pi, gb); else pi = -1;
+                }
+            }
+            // no more units: the next slot gets an empty unit that stops the consumers
+            if (!slot_free(j)) {
+                atomicOr(a.err, kErrEmptyTimeout);
+                drain(j);
+                return;
+            }
+            info[j % S].pi = -1;
+            mbar_arrive(&full[j % S]);
+            // the last CTA to finish taking blocks leaves the counters zeroed
+            if (atomicAdd(&a.dyn[1], 1u) == (unsigned)a.ctas - 1) {
+                atomicExch(&a.dyn[0], 0u);
+                atomicExch(&a.dyn[1], 0u);
+            }
+            return;
+        }
         const int64_t nfill = i64min(S, nunits);
 #pragma unroll
         for (int j = 0; j < S; ++j)
@@ -647,9 +756,7 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
         for (int64_t j = nfill; j < nunits; ++j) {
             if (*abort_flag || !mbar_wait(&empty[sl], ph, kWaitLimitNs)) {
                 atomicOr(a.err, kErrEmptyTimeout);
-                // let the copies already issued land before the CTA can exit
-                for (int64_t k = i64max(0, j - S); k < j; ++k)
-                    mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), kWaitLimitNs);
+                drain(j);
                 return;
             }
             const uint8_t *xs;
@@ -677,13 +784,20 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
     for (int r = 0; r < C::GPW; ++r) acc[r] = 0.f;
     int sl = 0;
     uint32_t ph = 0;  // phase parity of unit j on `full`
-    for (int64_t j = 0; j < nunits; ++j) {
+    for (int64_t j = 0; dyn || j < nunits; ++j) {
         if (!mbar_wait(&full[sl], ph, kWaitLimitNs)) {
             if (lane == 0) {
                 atomicOr(a.err, kErrFullTimeout);
                 *abort_flag = 1;
             }
             return;
+        }
+        if (dyn) {  // the producer says which unit the slot holds
+            const SlotInfo inf = info[sl];
+            if (inf.pi < 0) break;
+            pi = inf.pi;
+            c = inf.c;
+            gb = inf.gb;
         }
         const StreamProb &p = a.p[pi];
         const int64_t g0 = gb * L::GPU + warp;  // this warp's first group in the problem
@@ -707,7 +821,7 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
                 const int64_t g = g0 + r * kStreamWarps;
                 const int slot = warp + r * kStreamWarps;  // the group's place in the unit
                 const int64_t n = g * kRowsPerGroup + lane;
-                if (u0 >= beg && u1 < end) {  // the whole group is in this CTA
+                if (dyn || (u0 >= beg && u1 < end)) {  // the whole group is in this CTA
                     if (n < p.N) p.y[n] = acc[r];
                 } else {
                     // split between CTAs: publish; the last CTA to arrive adds up

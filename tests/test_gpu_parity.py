@@ -334,3 +334,49 @@ def test_bounded_wait_times_out(lean):
     y_ref, bound = oracle.qmatmul(fmt, W, x, N, K)
     check_close(yd.cpu().numpy().astype(np.float64), y_ref, bound, "after self-test")
     assert lean.lean_device_error(True) == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+@pytest.mark.parametrize("planes", [0, 1], ids=["fp32_x", "x_planes"])
+def test_batch_run_time_handout(lean, fmt, planes):
+    """A batch with at least three group blocks (256 rows) per CTA slot takes
+    whole group blocks at run time, largest first: every row is right, two
+    calls on one workspace agree bit for bit, and the counters end at zero."""
+    torch = torch_cuda()
+    be = syn.BLOCK_ELEMS[fmt]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nprob = 256
+    per = -(-3 * 2 * sms // nprob) + 1  # group blocks per problem
+    items, keep, refs, groups = [], [], [], 0
+    for i in range(nprob):
+        N = 256 * per - (0 if i % 3 else 200)  # some problems end in a partial block
+        K = be * (1 + i % 4) * (1 if fmt == syn.Q6_K else 2)
+        W, x = syn.make_problem(fmt, N, K, 1, seed=(33, fmt, i))
+        Wd = lean.upload_packed(fmt, W, N, K)
+        xd = torch.from_numpy(x).cuda()
+        yd = torch.full((N,), float("nan"), device="cuda")
+        keep += [Wd, xd, yd]
+        items.append((Wd, xd, yd, N, K))
+        refs.append(oracle.qmatmul(fmt, W, x, N, K))
+        groups += (N + 31) // 32
+    probs = lean.make_problems(items)
+    nb = lean.lean_batch_workspace_bytes(fmt, probs)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    flags = lean.LEAN_FLAG_EARLY_WEIGHTS | (lean.LEAN_FLAG_X_PLANES if planes else 0)
+    outs = []
+    for rep in range(2):
+        for it in items:
+            it[2].fill_(float("nan"))
+        lean.lean_qmatmul_batch(fmt, probs, flags, ws, nb)
+        torch.cuda.synchronize()
+        ys = []
+        for (Wd, xd, yd, N, K), (y_ref, bound) in zip(items, refs):
+            y = yd.cpu().numpy().astype(np.float64)[None, :]
+            check_close(y, y_ref, bound, "handout N=%d K=%d" % (N, K))
+            ys.append(y)
+        outs.append(np.concatenate(ys, axis=1))
+    assert np.array_equal(outs[0], outs[1])
+    # arrival counters and the two hand-out counters: the workspace's tail
+    cnt_bytes = (4 * (groups + 2) + 255) // 256 * 256
+    assert int(ws[nb - cnt_bytes:].count_nonzero()) == 0
+    assert lean.lean_device_error(True) == 0
