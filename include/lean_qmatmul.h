@@ -196,7 +196,12 @@ lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_de
 /* Several independent M = 1 products of one format in a single launch, for a
  * decode step whose linears do not depend on each other (or one dependency
  * level of a layer, e.g. q/k/v or gate/up).  Their row-group steps are
- * concatenated and streamed by one persistent grid. */
+ * concatenated and streamed by one persistent grid.  With a workspace and at
+ * least three 256-row blocks per CTA of the grid (a whole decode step), the
+ * CTAs take whole 256-row blocks at run time, largest first, from two
+ * counters at the end of the workspace (left at zero by every call); each
+ * row is still summed in one fixed order, so results do not depend on the
+ * schedule. */
 #define LEAN_MAX_BATCH 256
 typedef struct {
     const void *W;  /* device, packed by lean_pack, 16-byte aligned         */
