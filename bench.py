@@ -209,32 +209,44 @@ class DeviceWorkload:
         # one workspace, zeroed once: consecutive calls on the stream share it
         fmt0 = self.lins[0].fmt
         self.batch = None
+        self.batch_host = None
+        self.planes = False
         if (len(self.lins) > 1 and len(self.lins) <= lean.LEAN_MAX_BATCH
                 and all(l.M == 1 and l.fmt == fmt0 for l in self.lins)):
-            self.batch = []
-            for c in range(self.copies):
-                items = [(self.W[c][i], self.x.data_ptr() + 4 * self.x_off[i],
-                          self.y.data_ptr() + 4 * self.y_off[i], l.N, l.K)
-                         for i, l in enumerate(self.lins)]
-                self.batch.append(lean.make_problems(items))
+            # with a workspace, integer formats streaming >= 32 MiB of weights
+            # get a first kernel that writes x as integer planes
+            self.planes = fmt0 != syn.Q6_K and sum(p.nbytes for p in packed) >= 32 << 20
+
+            def problems(c, x_base, y_base):
+                return lean.make_problems([(self.W[c][i], x_base + 4 * self.x_off[i],
+                                            y_base + 4 * self.y_off[i], l.N, l.K)
+                                           for i, l in enumerate(self.lins)])
+            self.batch = [problems(c, self.x.data_ptr(), self.y.data_ptr())
+                          for c in range(self.copies)]
+            if self.planes:
+                # the plane path reads x and writes y with plain loads and
+                # stores, so the same call can take the pinned host buffers
+                # themselves (zero-copy over the host link)
+                self.batch_host = [problems(c, self.x_host.data_ptr(), self.y_host.data_ptr())
+                                   for c in range(self.copies)]
             self.ws_bytes = lean.lean_batch_workspace_bytes(fmt0, self.batch[0])
         else:
             self.ws_bytes = max(lean.lean_qmatmul_workspace_bytes(l.fmt, l.N, l.K, l.M)
                                 for l in self.lins)
         self.ws = torch.zeros(max(256, self.ws_bytes), dtype=torch.uint8, device=device)
 
-    def run_step(self, copy, stream):
+    def run_step(self, copy, stream, host=False):
         """One pass over every linear: a single batched launch when all linears
-        are M = 1 products of one format, otherwise one call per linear."""
+        are M = 1 products of one format, otherwise one call per linear.
+        host: the batch whose x and y are the pinned host buffers."""
         lean = self.lean
         if self.batch is not None:
-            lean.lean_qmatmul_batch(self.lins[0].fmt, self.batch[copy], self.flags, self.ws,
-                                    self.ws_bytes, stream)
-            # with a workspace, integer formats streaming >= 32 MiB of weights get
-            # a first kernel that writes x as integer planes
-            planes = (self.lins[0].fmt != syn.Q6_K
-                      and sum(p.nbytes for p in self.packed_sizes) >= 32 << 20)
-            self.launches_per_step = 2 if planes else 1
+            # host buffers only ever go down the plane path (asked for explicitly)
+            flags = self.flags | (lean.LEAN_FLAG_X_PLANES if host else 0)
+            lean.lean_qmatmul_batch(self.lins[0].fmt,
+                                    (self.batch_host if host else self.batch)[copy],
+                                    flags, self.ws, self.ws_bytes, stream)
+            self.launches_per_step = 2 if self.planes else 1
             return
         n = 0
         tc_min = lean.lean_tensor_core_min_m()
@@ -252,14 +264,14 @@ class DeviceWorkload:
                 n += 2                        # x split + tensor-core product
         self.launches_per_step = n
 
-    def capture(self, stream):
+    def capture(self, stream, host=False):
         torch = self.torch
         graphs = []
         for c in range(self.copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(stream):
                 with torch.cuda.graph(g, stream=stream):
-                    self.run_step(c, stream)
+                    self.run_step(c, stream, host)
             graphs.append(g)
         return graphs
 
@@ -325,27 +337,45 @@ def time_gpu(args, wl):
     sampler.stop()
     clocks = sampler.summary(t0, t1)
 
-    # end to end: pinned host x -> device, the step, y -> pinned host, every step
+    # end to end: every step takes x from pinned host memory and leaves y in
+    # pinned host memory.  On the plane path the call itself is given the host
+    # buffers (the kernels read x and write y across the host link); otherwise
+    # x is copied in and y out around the call.
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e_steps = max(3, min(args.steps, 200))
-    with torch.cuda.stream(stream):
-        for s in range(2):
+    zero_copy = dw.batch_host is not None
+    if zero_copy:
+        hgraphs = dw.capture(stream, host=True)
+
+    def e2e_step(s):
+        if zero_copy:
+            hgraphs[s % dw.copies].replay()
+        else:
             dw.x.copy_(dw.x_host, non_blocking=True)
             graphs[s % dw.copies].replay()
             dw.y_host.copy_(dw.y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for s in range(2):
+            e2e_step(s)
     torch.cuda.synchronize()
     barrier()
     e0.record(stream)
     with torch.cuda.stream(stream):
         for s in range(e_steps):
-            dw.x.copy_(dw.x_host, non_blocking=True)
-            graphs[s % dw.copies].replay()
-            dw.y_host.copy_(dw.y, non_blocking=True)
+            e2e_step(s)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e_steps
+    e2e_same = None
+    if zero_copy:
+        # the host-buffer call gives bit for bit what the device-buffer call gives
+        with torch.cuda.stream(stream):
+            graphs[0].replay()
+        torch.cuda.synchronize()
+        e2e_same = bool(np.array_equal(dw.y_host.numpy(), dw.y.cpu().numpy()))
 
     if ws > 1:
         import torch.distributed as dist
@@ -360,7 +390,8 @@ def time_gpu(args, wl):
     return {"ms": ms, "e2e_ms": e2e_ms, "clocks": clocks, "launches": dw.launches_per_step,
             "kernel": kernel,
             "copies": dw.copies, "spot_ok": spot, "h2d": dw.x_host.numel() * 4,
-            "d2h": dw.y_host.numel() * 4, "l2": l2}
+            "d2h": dw.y_host.numel() * 4, "l2": l2, "e2e_zero_copy": zero_copy,
+            "e2e_same": e2e_same}
 
 
 # ----------------------------------------------------------------- CPU arm ---
@@ -477,7 +508,12 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": job_gbs(alg_bytes, r["e2e_ms"], ws), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                "ms_per_step": r["e2e_ms"]},
+                "ms_per_step": r["e2e_ms"],
+                "transfer": ("the call takes the pinned host x and y buffers; its kernels read "
+                             "x and write y across the host link (zero-copy)"
+                             if r["e2e_zero_copy"] else
+                             "cudaMemcpyAsync of x in and y out around the call, every step"),
+                "matches_device_buffers": r["e2e_same"]},
         "gpu_launches": r["launches"] * args.steps,
         "clocks": r["clocks"],
         "spot_check_vs_oracle": r["spot_ok"],

@@ -216,7 +216,12 @@ int64_t lean_batch_workspace_bytes(int fmt, int count, const lean_problem *probl
 /* problems: host array of `count` (1..LEAN_MAX_BATCH) descriptors, read during
  * the call only.  workspace / workspace_bytes / flags as for lean_qmatmul_ws
  * (workspace may be NULL).  Outputs of different problems must not overlap
- * each other or any input. */
+ * each other or any input.  On the x-plane path (Q4_0 / Q8_0 / I8_B64 with a
+ * workspace and LEAN_FLAG_X_PLANES) x is read and y written only with plain
+ * loads and stores, so x and y may also be pinned host memory that the
+ * device addresses directly (cudaHostAlloc / cudaHostRegister under unified
+ * addressing): the kernels then move them across the host link themselves.
+ * W and the workspace must be device memory. */
 lean_status lean_qmatmul_batch(int fmt, int count, const lean_problem *problems,
                                unsigned flags, void *workspace, int64_t workspace_bytes,
                                void *stream);

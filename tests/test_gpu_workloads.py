@@ -85,6 +85,38 @@ def test_decode_stack_batch_x_planes():
     assert lean.lean_device_error(True) == 0
 
 
+def test_decode_stack_batch_host_buffers():
+    """The same decode step with x and y in pinned host memory, passed to the
+    call as they are (the x-plane path reads x and writes y with plain loads
+    and stores, across the host link): every output against the oracle, and
+    bit for bit what device buffers give."""
+    torch = torch_cuda()
+    from block_quantized_weight_dot_gb300 import lean
+    stack = syn.smollm2_360m_decode_stack()
+    dev, host, keep, refs = [], [], [], []
+    for lin in stack.linears:
+        W, x = lin.make()
+        Wd = lean.upload_packed(lin.fmt, W, lin.N, lin.K)
+        xh = torch.from_numpy(np.ascontiguousarray(x.reshape(-1))).pin_memory()
+        yh = torch.full((lin.N,), float("nan")).pin_memory()
+        xd, yd = xh.cuda(), torch.full((lin.N,), float("nan"), device="cuda")
+        keep += [Wd, xh, yh, xd, yd]
+        host.append((Wd, xh, yh, lin.N, lin.K))
+        dev.append((Wd, xd, yd, lin.N, lin.K))
+        refs.append(oracle.qmatmul(lin.fmt, W, x, lin.N, lin.K, threads=THREADS))
+    nb = lean.lean_batch_workspace_bytes(syn.Q4_0, lean.make_problems(dev))
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    flags = lean.LEAN_FLAG_EARLY_WEIGHTS | lean.LEAN_FLAG_X_PLANES
+    for items in (host, dev):
+        lean.lean_qmatmul_batch(syn.Q4_0, lean.make_problems(items), flags, ws, nb)
+    torch.cuda.synchronize()
+    for lin, h, d, (y_ref, bound) in zip(stack.linears, host, dev, refs):
+        yh = h[2].numpy().astype(np.float64)
+        check_close(yh[None, :], y_ref, bound, "host buffers " + lin.name)
+        assert np.array_equal(yh, d[2].cpu().numpy().astype(np.float64)), lin.name
+    assert lean.lean_device_error(True) == 0
+
+
 @pytest.mark.parametrize("fmt", [syn.Q8_0, syn.I8_B64], ids=["q8_0", "i8_b64"])
 def test_tinyllama_full(fmt):
     torch_cuda()
