@@ -58,6 +58,10 @@ def _load():
             lib.oracle_qmatmul_pairs.argtypes = [c_int, vp, vp, c_i64, c_i64, c_i64, c_i64,
                                                  vp, vp, vp, vp]
             lib.oracle_qmatmul_pairs.restype = c_int
+            lib.oracle_quantize.argtypes = [c_int, vp, vp, c_i64, c_i64]
+            lib.oracle_quantize.restype = c_int
+            lib.oracle_double_to_fp16.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_fp16.restype = c_int
             _lib = lib
     return _lib
 
@@ -126,3 +130,21 @@ def qmatmul_pairs(fmt: int, W: np.ndarray, x: np.ndarray, N: int, K: int,
     if rc:
         raise ValueError("oracle_qmatmul_pairs failed (%d)" % rc)
     return y, b
+
+
+def double_to_fp16(v: float) -> int:
+    """binary16 bits of the value nearest to v (ties to even), or -1."""
+    return _load().oracle_double_to_fp16(float(v))
+
+
+def quantize(fmt: int, w: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Canonical blocks of fp32 w[N][K] by the quantizer reading in
+    lean_oracle.c (Q4_0, Q8_0, I8_B64); ValueError if it rejects the input."""
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(N, K)
+    be, bb = block_elems(fmt), block_bytes(fmt)
+    if be == 0 or K % be:
+        raise ValueError("bad format or K")
+    out = np.zeros(N * (K // be) * bb, dtype=np.uint8)
+    if _load().oracle_quantize(fmt, _ptr(w), _ptr(out), N, K):
+        raise ValueError("oracle_quantize rejected the input")
+    return out

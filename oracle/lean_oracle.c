@@ -239,3 +239,144 @@ int oracle_qmatmul_pairs(int fmt, const uint8_t *W, const float *x, int64_t N, i
     }
     return 0;
 }
+
+/* ---- float -> block quantizers (packing helpers) ------------------------------
+ *
+ * The pages quantize weights at load time ("oxinfer" crate page, How it works:
+ * quant.rs gives Q8 blocks of 32 weights with one scale and Q4_0 two nibbles
+ * per byte with an f16 scale; "wgpu-llm" README, INT8 mode: a quantizer with
+ * block size 64) but state no rounding rule.  The reading taken here:
+ *
+ *   Q8_0, INT8-B64: d = the binary16 value nearest to max|w| / 127 (ties to
+ *     even); q = the integer nearest to w / d (ties away from zero), clamped
+ *     to -127..127.  A block of zeros, or one whose d rounds to zero, stores
+ *     d = +0 and q = 0.
+ *   Q4_0: m = the element of largest |w| (the first one when several tie);
+ *     d = the binary16 value nearest to m / -8, so that m itself comes back
+ *     as d * (0 - 8); q = (integer nearest to w / d, ties away from zero) + 8,
+ *     clamped to 0..15.  d = +0 gives q = 8 (value 0).
+ *
+ * Everything is computed in double: w / d of two floats is correctly rounded
+ * there, and that rounding can never move a quotient onto or off a half-way
+ * point, so the integer chosen is the one the exact quotient gives.  A
+ * non-finite input, or a scale beyond the largest binary16 value (65504),
+ * fails the call. */
+
+/* binary16 bits of the value nearest to v (ties to even), written from the
+ * format: values k * 2^-24 below 2^-14 (subnormal), k * 2^(e-10) in
+ * [2^e, 2^(e+1)).  Returns -1 if v is not finite or rounds past 65504. */
+static int double_to_fp16_bits(double v, uint16_t *bits)
+{
+    if (!isfinite(v)) return -1;
+    int sign = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    double spacing;
+    if (a < ldexp(1.0, -14)) {
+        spacing = ldexp(1.0, -24);
+    } else {
+        int e;
+        frexp(a, &e);                      /* a in [2^(e-1), 2^e) */
+        spacing = ldexp(1.0, e - 1 - 10);
+    }
+    double k = a / spacing;                /* exact: spacing is a power of two */
+    double kf = floor(k);
+    double rest = k - kf;
+    if (rest > 0.5 || (rest == 0.5 && fmod(kf, 2.0) == 1.0)) kf += 1.0;
+    double r = kf * spacing;               /* exact */
+    if (r > 65504.0) return -1;
+    uint16_t h;
+    if (r == 0.0) {
+        h = 0;
+    } else if (r < ldexp(1.0, -14)) {
+        h = (uint16_t)(r / ldexp(1.0, -24));
+    } else {
+        int e;
+        double f = frexp(r, &e);           /* r = f * 2^e, f in [0.5, 1) */
+        int ex = e - 1;                    /* r = (2f) * 2^ex, 2f in [1, 2) */
+        int frac = (int)((2.0 * f - 1.0) * 1024.0);
+        h = (uint16_t)(((ex + 15) << 10) | frac);
+    }
+    if (sign) h |= 0x8000;                 /* a negative value that rounds to 0 gives -0 */
+    *bits = h;
+    return 0;
+}
+
+/* the integer nearest to t, ties away from zero (exact for |t| < 2^52) */
+static double round_half_away(double t)
+{
+    double a = fabs(t);
+    double f = floor(a);
+    if (a - f >= 0.5) f += 1.0;
+    return t < 0 ? -f : f;
+}
+
+static int quantize_block(int fmt, const float *w, uint8_t *blk)
+{
+    int be = oracle_block_elems(fmt);
+    for (int j = 0; j < be; ++j)
+        if (!isfinite(w[j])) return -1;
+    uint16_t dbits = 0;
+    if (fmt == ORACLE_Q4_0) {
+        double m = 0.0;
+        for (int j = 0; j < be; ++j)
+            if (fabs((double)w[j]) > fabs(m)) m = (double)w[j];
+        if (m != 0.0 && double_to_fp16_bits(m / -8.0, &dbits)) return -1;
+        if ((dbits & 0x7fff) == 0) dbits = 0;  /* a scale that rounds to zero is stored as +0 */
+        double d = oracle_fp16_to_double(dbits);
+        blk[0] = (uint8_t)(dbits & 0xff);
+        blk[1] = (uint8_t)(dbits >> 8);
+        memset(blk + 2, 0, 16);
+        for (int j = 0; j < be; ++j) {
+            double q = 8.0;
+            if (d != 0.0) {
+                q = round_half_away((double)w[j] / d) + 8.0;
+                if (q < 0.0) q = 0.0;
+                if (q > 15.0) q = 15.0;
+            }
+            int qi = (int)q;
+            if (j < 16) blk[2 + j] |= (uint8_t)qi;
+            else blk[2 + j - 16] |= (uint8_t)(qi << 4);
+        }
+        return 0;
+    }
+    if (fmt == ORACLE_Q8_0 || fmt == ORACLE_I8_B64) {
+        double amax = 0.0;
+        for (int j = 0; j < be; ++j)
+            if (fabs((double)w[j]) > amax) amax = fabs((double)w[j]);
+        if (amax != 0.0 && double_to_fp16_bits(amax / 127.0, &dbits)) return -1;
+        double d = oracle_fp16_to_double(dbits);  /* amax / 127 >= 0: never -0 */
+        blk[0] = (uint8_t)(dbits & 0xff);
+        blk[1] = (uint8_t)(dbits >> 8);
+        for (int j = 0; j < be; ++j) {
+            double q = 0.0;
+            if (d != 0.0) {
+                q = round_half_away((double)w[j] / d);
+                if (q < -127.0) q = -127.0;
+                if (q > 127.0) q = 127.0;
+            }
+            blk[2 + j] = (uint8_t)(int8_t)(int)q;
+        }
+        return 0;
+    }
+    return -1;  /* Q6_K has no quantizer here */
+}
+
+/* w[N][K] fp32 -> canonical blocks (row-major, blocks along K).  0 on
+ * success, -1 on a bad format / shape or an input the reading rejects. */
+int oracle_quantize(int fmt, const float *w, uint8_t *canon, int64_t N, int64_t K)
+{
+    int be = oracle_block_elems(fmt), bb = oracle_block_bytes(fmt);
+    if (fmt == ORACLE_Q6_K || be == 0 || N <= 0 || K <= 0 || K % be != 0) return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < K / be; ++b)
+            if (quantize_block(fmt, w + n * K + b * be, canon + (n * (K / be) + b) * bb))
+                return -1;
+    return 0;
+}
+
+/* For the tests: binary16 bits of the value nearest to v, or -1. */
+int oracle_double_to_fp16(double v)
+{
+    uint16_t h;
+    return double_to_fp16_bits(v, &h) ? -1 : (int)h;
+}
