@@ -23,6 +23,10 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompil
               "--expt-relaxed-constexpr"] + ARCH
 SOURCES = ["lean_qmatmul.cu", "pack.cpp", "qmm_q4_0.cu", "qmm_q8_0.cu", "qmm_i8_b64.cu", "qmm_q6_k.cu",
            "qmm_fixed_ws.cu"]
+# host-only helpers (no CUDA), compiled by the host C++ compiler
+HOST = os.path.join(HERE, "host")
+HOST_SOURCES = ["quant.cpp"]
+HOST_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-ffp-contract=off", "-pthread"]
 
 
 def nvcc() -> str:
@@ -34,7 +38,9 @@ def nvcc() -> str:
 
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(ROOT, "include", "lean_qmatmul.h"))
+    files += [os.path.join(HOST, f) for f in os.listdir(HOST)]
+    inc = os.path.join(ROOT, "include")
+    files += [os.path.join(inc, f) for f in os.listdir(inc)]
     return files
 
 
@@ -54,15 +60,27 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
+def _compile_host(src: str) -> str:
+    obj = os.path.join(BUILD, "host_" + os.path.basename(src) + ".o")
+    cxx = os.environ.get("CXX") or shutil.which("g++") or "c++"
+    cmd = [cxx] + HOST_FLAGS + ["-c", os.path.join(HOST, src), "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("host compile failed for %s:\n%s\n%s" % (src, " ".join(cmd), r.stderr))
+    return obj
+
+
 def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     """Compile every source for sm_103a and link liblean_qmatmul.so."""
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES) + len(HOST_SOURCES)) as ex:
+        dev = [ex.submit(_compile, s, extra) for s in SOURCES]
+        host = [ex.submit(_compile_host, s) for s in HOST_SOURCES]
+        objs = [f.result() for f in dev + host]
     tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"]
+    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))

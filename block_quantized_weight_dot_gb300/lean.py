@@ -1,4 +1,5 @@
-"""ctypes binding of ``liblean_qmatmul.so`` (C ABI in ``include/lean_qmatmul.h``).
+"""ctypes binding of ``liblean_qmatmul.so`` (C ABI in ``include/lean_qmatmul.h`` and
+``include/lean_quant.h``).
 
 Argument marshalling only: every computation of the product runs in the CUDA
 library.  Functions keep the C names.  Buffers may be given as torch tensors
@@ -41,6 +42,7 @@ SIGNATURES = {
     "lean_qmatmul_batch": (_int, [_int, _int, _vp, ctypes.c_uint, _vp, _i64, _vp]),
     "lean_device_error": (ctypes.c_uint, [_int]),
     "lean_wait_selftest": (_int, [ctypes.c_uint, _vp]),
+    "lean_quantize": (_int, [_int, _vp, _vp, _i64, _i64, _int]),
     "lean_qmatmul_fixed_ws": (_int, [_int, _vp, _vp, _vp, _i64, _i64, ctypes.c_uint, _vp]),
     "lean_fixed_workspace_bytes": (_i64, []),
     "lean_status_str": (ctypes.c_char_p, [_int]),
@@ -229,6 +231,19 @@ def lean_fixed_workspace_bytes() -> int:
 def lean_device_error(clear: bool = True) -> int:
     """Device error word (non-zero: a kernel's bounded wait timed out)."""
     return _lib.lean_device_error(1 if clear else 0)
+
+
+def lean_quantize(fmt: int, w, N: int, K: int, threads: int = 0):
+    """Canonical blocks (uint8 array, ready for lean_pack) of fp32 w[N][K]
+    quantized on the host to Q4_0, Q8_0 or I8_B64 (rule in lean_quant.h)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    if w.size != N * K:
+        raise ValueError("w has %d elements, expected %d" % (w.size, N * K))
+    nbytes = lean_canonical_bytes(fmt, N, K)
+    out = np.zeros(max(nbytes, 1), dtype=np.uint8)  # a bad shape is reported by the call
+    _check("lean_quantize", _lib.lean_quantize(fmt, w.ctypes.data, out.ctypes.data, N, K,
+                                                threads))
+    return out[:nbytes]
 
 
 def lean_wait_selftest(limit_us: int, stream=None) -> None:
