@@ -422,6 +422,33 @@ def time_oracle(inputs, n_per_step, budget_s, start=0):
             "seconds": elapsed, "linears": n_lin, "next": i}
 
 
+# ------------------------------------------------------ host quantizer ---
+
+def time_quantizer(reps=5):
+    """lean_quantize (host threads, no GPU) on seeded fp32 weights at the
+    Qwen2.5-3B FFN shapes: one JSON line per format on stdout."""
+    from block_quantized_weight_dot_gb300 import lean
+    cores = len(os.sched_getaffinity(0))
+    rng = np.random.default_rng((0, 9))
+    mats = [(rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+            for N, K in syn.QWEN25_3B_FFN_SHAPES]
+    for fmt in (syn.Q4_0, syn.Q8_0, syn.I8_B64):
+        lean.lean_quantize(fmt, mats[0], *mats[0].shape)  # first-touch of the output pages
+        best = None
+        for _ in range(reps):
+            t = time.perf_counter()
+            for w in mats:
+                lean.lean_quantize(fmt, w, *w.shape)
+            dt = time.perf_counter() - t
+            best = dt if best is None else min(best, dt)
+        params = sum(w.size for w in mats)
+        print(json.dumps({"quantizer": syn.FORMAT_NAMES[fmt], "params": params,
+                          "seconds": best, "params_per_s": params / best,
+                          "input_gb_per_s": 4 * params / best / 1e9, "threads": cores,
+                          "shapes": [list(w.shape) for w in mats],
+                          "timing": "best of %d, host wall clock" % reps}), flush=True)
+
+
 # -------------------------------------------------------------------- main ---
 
 def main():
@@ -434,7 +461,12 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="also time every workload (stderr)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quantize", action="store_true",
+                    help="time the host quantizer lean_quantize instead (no GPU)")
     args = ap.parse_args()
+    if args.quantize:
+        time_quantizer()
+        return
     ws, rank, local = dist_env()
     wl = workload_by_name(args.workload)
     peak, peak_kind = measured_peaks()

@@ -13,7 +13,9 @@
 //   a scale that rounds to zero is stored as +0 with every value 0.
 // The quotients are taken in double, where w / d is correctly rounded and
 // cannot land on or leave a half-way point, so the codes are those of the
-// exact quotients.  Host code only: no kernel depends on this file.
+// exact quotients; |w / d| stays below 2 * 127 (the scale is at least half
+// of max|w| / 127 or |m| / 8 once rounded), far inside the integer
+// conversion used to round.  Host code only: no kernel depends on this file.
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -59,6 +61,14 @@ bool half_bits(double v, uint16_t &out) {
     return true;
 }
 
+// nearest integer to t, ties away from zero, for |t| < 2^31: the conversion
+// truncates toward zero, and t - trunc(t) is exact
+inline double round_away(double t) {
+    const double r = (double)(int64_t)t;
+    const double f = t - r;
+    return f >= 0.5 ? r + 1.0 : (f <= -0.5 ? r - 1.0 : r);
+}
+
 double half_value(uint16_t h) {
     const int e = (h >> 10) & 0x1f, f = h & 0x3ff;
     const double a = e == 0 ? std::ldexp((double)f, -24) : std::ldexp((double)(f + 1024), e - 25);
@@ -89,14 +99,14 @@ bool quantize_block(int fmt, const float *w, uint8_t *blk) {
     if (fmt == LEAN_Q4_0) {
         uint8_t q[32];
         for (int j = 0; j < 32; ++j) {
-            double t = d == 0.0 ? 8.0 : std::round((double)w[j] / d) + 8.0;
+            double t = d == 0.0 ? 8.0 : round_away((double)w[j] / d) + 8.0;
             t = t < 0.0 ? 0.0 : t > 15.0 ? 15.0 : t;
             q[j] = (uint8_t)t;
         }
         for (int j = 0; j < 16; ++j) blk[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
     } else {
         for (int j = 0; j < be; ++j) {
-            double t = d == 0.0 ? 0.0 : std::round((double)w[j] / d);
+            double t = d == 0.0 ? 0.0 : round_away((double)w[j] / d);
             t = t < -127.0 ? -127.0 : t > 127.0 ? 127.0 : t;
             blk[2 + j] = (uint8_t)(int8_t)(int)t;
         }
