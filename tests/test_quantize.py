@@ -91,3 +91,28 @@ def test_errors(lean):
     assert f(syn.Q8_0, big.ctypes.data, buf.ctypes.data, 1, 32, 1) == lean.LEAN_ERR_SHAPE
     with pytest.raises(lean.LeanError):
         lean.lean_quantize(syn.Q8_0, np.ones((2, 63), np.float32), 2, 63)
+
+
+def test_any_finite_block_matches_oracle(lean):
+    """Property: for any finite float32 block the product and the oracle agree
+    byte for byte, or both refuse it (a scale past 65504)."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    floats = st.floats(allow_nan=False, allow_infinity=False, width=32)
+
+    @hyp.settings(max_examples=300, deadline=None)
+    @hyp.given(fmt=st.sampled_from(FMTS), data=st.data())
+    def check(fmt, data):
+        be = syn.BLOCK_ELEMS[fmt]
+        w = np.array(data.draw(st.lists(floats, min_size=be, max_size=be)), np.float32)
+        try:
+            want = oracle.quantize(fmt, w, 1, be)
+        except ValueError:
+            want = None
+        if want is None:
+            with pytest.raises(lean.LeanError):
+                lean.lean_quantize(fmt, w, 1, be)
+        else:
+            assert lean.lean_quantize(fmt, w, 1, be).tobytes() == want.tobytes()
+
+    check()
