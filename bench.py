@@ -391,6 +391,7 @@ def time_gpu(args, wl):
             "kernel": kernel,
             "copies": dw.copies, "spot_ok": spot, "h2d": dw.x_host.numel() * 4,
             "d2h": dw.y_host.numel() * 4, "l2": l2, "e2e_zero_copy": zero_copy,
+            "planes": dw.planes,
             "e2e_same": e2e_same}
 
 
@@ -526,7 +527,9 @@ def main():
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        # the x-plane path sums integer products in int32 (dp4a) and combines them in fp32
+        "dtype": "int32+fp32" if r["planes"] else "fp32", "data": "synthetic",
         "config": config,
         "linears_per_s": linears_per_s,
         "frac_of_hbm_peak": gbs / ws / peak,
