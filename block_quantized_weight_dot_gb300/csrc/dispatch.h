@@ -63,8 +63,10 @@ lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int6
 
 // The M = 1 product with a workspace; planes = false keeps x in fp32 (the
 // layout without a plane region, as the fixed array of lean_qmatmul_fixed_ws).
+// clear_counters: once every argument has been checked, zero the arrival
+// counters on the stream before the product (a rejected call queues nothing).
 lean_status qmatmul_m1_ws(int fmt, const void *W, const float *x, float *y, int64_t N,
                           int64_t K, unsigned flags, void *ws, int64_t ws_bytes, bool planes,
-                          cudaStream_t stream);
+                          bool clear_counters, cudaStream_t stream);
 
 }  // namespace lean

@@ -443,7 +443,7 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
                 xa.p[i].pad = 0;
             }
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)((max_nb + 8 * kXprepBlocks - 1) / (8 * kXprepBlocks)),
+            cfg.gridDim = dim3((unsigned)((max_nb + kXprepCtaBlocks - 1) / kXprepCtaBlocks),
                                (unsigned)n, 1);
             cfg.blockDim = dim3(256, 1, 1);
             cfg.stream = stream;

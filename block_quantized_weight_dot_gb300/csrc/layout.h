@@ -35,8 +35,8 @@ constexpr int kVec = 16;                       // bytes per row per vector
 constexpr int kVecBytes = kVec * kRowsPerGroup;  // 512 bytes per vector
 constexpr int kBlocksPerStep = 8;
 // x of the M = 1 product as integer planes: bytes per 32-element block
-// (a 16-byte header, then three 32-byte planes)
-constexpr int kXqBlockBytes = 112;
+// (a 32-byte header, then four 32-byte planes)
+constexpr int kXqBlockBytes = 160;
 
 enum Fmt { Q4_0 = 0, Q8_0 = 1, I8_B64 = 2, Q6_K = 3 };
 

@@ -86,12 +86,19 @@ lean_status check_product(int fmt, const void *W, const float *x, const float *y
 namespace lean {
 lean_status qmatmul_m1_ws(int fmt, const void *W, const float *x, float *y, int64_t N,
                           int64_t K, unsigned flags, void *ws, int64_t ws_bytes, bool planes,
-                          cudaStream_t stream) {
+                          bool clear_counters, cudaStream_t stream) {
     Geom g;
     lean_status st = check_product(fmt, W, x, y, N, K, 1, flags, &g);
     if (st != LEAN_OK) return st;
-    if (ws && !aligned(ws, 256)) return LEAN_ERR_ALIGN;
+    if (!ws || !aligned(ws, 256)) return ws ? LEAN_ERR_ALIGN : LEAN_ERR_NULL;
+    const WorkspaceLayout wl = workspace_layout(g.groups, planes ? xq_bytes(fmt, K) : 0);
+    if (ws_bytes < wl.total) return LEAN_ERR_SHAPE;
     cudaGetLastError();
+    // every argument is valid: only now may anything be queued on the stream
+    if (clear_counters &&
+        cudaMemsetAsync(static_cast<uint8_t *>(ws) + wl.cnt_off, 0, (size_t)(g.groups * 4),
+                        stream) != cudaSuccess)
+        return LEAN_ERR_CUDA;
     HostProb hp = {(const uint8_t *)W, x, y, g};
     return dispatch_stream(fmt, &hp, 1, flags, ws, ws_bytes, planes, stream);
 }

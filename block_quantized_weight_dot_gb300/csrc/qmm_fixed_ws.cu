@@ -62,12 +62,10 @@ lean_status lean_qmatmul_fixed_ws(int fmt, const void *W_packed_dev, const float
     void *ws = fixed_workspace();
     if (!ws) return LEAN_ERR_CUDA;
     // The counters must start at zero; a call that gave up on a timeout could
-    // have left some set, so clear the ones this call uses.
-    if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + wl.cnt_off, 0, (size_t)(g.groups * 4),
-                        (cudaStream_t)stream) != cudaSuccess)
-        return LEAN_ERR_CUDA;
-    // x stays fp32 here: the array has no room for the x planes of every K
-    return qmatmul_m1_ws(fmt, W_packed_dev, x_dev, y_dev, N, K, flags, ws, wl.total, false,
+    // have left some set, so the call clears the ones it uses (after its
+    // arguments have been checked).  x stays fp32 here: the array has no room
+    // for the x planes of every K.
+    return qmatmul_m1_ws(fmt, W_packed_dev, x_dev, y_dev, N, K, flags, ws, wl.total, false, true,
                          (cudaStream_t)stream);
 }
 

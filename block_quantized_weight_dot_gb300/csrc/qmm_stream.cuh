@@ -12,16 +12,26 @@
 //    mbarrier;
 //  - with a workspace, the integer formats (Q4_0, Q8_0, I8_B64) take x as
 //    integer planes written once per call by xprep_kernel, so that the dot
-//    products run on dp4a: each 32-element block of x is
-//    scaled by a power of two 2^s chosen from its largest magnitude, rounded
-//    to integers X with |X| <= 2^22, and cut into three byte planes
-//    X = X2*2^16 + X1*2^8 + X0 (X2 signed).  Every plane's dp4a sum starts at
-//    -offset * (sum of the plane) (offset 8 for Q4_0, 128 for the stored int8
-//    bytes), so it ends as the exact integer sum of (q - offset) * plane; the
-//    three sums combine in fp32 and scale by d * 2^-s.  The rounding of x is
-//    at most 2^-23 of the block's largest |x|; a block of x = e_k stays exact.
-//    Without a workspace, and for Q6_K (whose 6-bit fields do not come out
-//    as bytes cheaply), x stays fp32 and the decode is the exact
+//    products run on dp4a: each 32-element block of x is scaled by a power of
+//    two 2^sf chosen from its largest magnitude, rounded to integers X with
+//    |X| < 2^31 and cut into four byte planes (X = X3*2^24 + X2*2^16 +
+//    X1*2^8 + X0, X3 signed).  Every plane's dp4a sum starts at -128 * (sum of
+//    the plane) and so ends as the exact integer sum of (q - offset) * plane
+//    (the raw weight bytes carry offset 128: int8 stored + 128, and Q4_0
+//    nibbles read as 16 * q with offset 16 * 8); the four sums combine exactly
+//    in integers, round once to fp32 and scale by d * 2^-sf.
+//    xprep_kernel checks every element: X is rounded on a grid 256 times
+//    coarser (lowest plane all zero) when that moves no element by more than
+//    2^-14 of itself, as for about 98 blocks in 100 of N(0,1) activations;
+//    else on the fine grid; and a block that even the fine grid cannot hold to
+//    2^-14 (a small value next to an outlier channel), or that holds an Inf or
+//    NaN, is marked, and the consumers take the exact fp32 dot for it from x
+//    itself.  The grid is decided per chunk (the x blocks of one unit), so the
+//    consumers branch once per chunk: three planes when all blocks are coarse,
+//    four otherwise, block by block only where a block is marked.  Each
+//    product w*x therefore errs by at most 2^-14 of |w*x| plus fp32 rounding,
+//    whatever x is.  Without a workspace, and for Q6_K (whose 6-bit fields do
+//    not come out as bytes cheaply), x stays fp32 and the decode is the exact
 //    mantissa-bias conversion with paired fp32 FMAs;
 //  - consumer warp w owns group w of every unit: lane r decodes row r from
 //    shared memory (conflict-free 16-byte reads, x as a broadcast read) and
@@ -153,10 +163,13 @@ struct StreamRing<Q4_0, true> {
 
 // x as integer planes (dp4a) for the integer formats
 template <int FMT> struct XPlanes { static constexpr bool on = FMT != Q6_K; };
-// One 32-element block of x in plane form: {init2, init1, init0, 2^-s} then
-// plane 2 (signed bytes), plane 1, plane 0, 32 bytes each.
+// One 32-element block of x in plane form: a 32-byte header {init3, init2,
+// init1, init0, scale, fine, 0, 0} (scale = 2^-s, times 1/16 for Q4_0; -1
+// marks a block that takes the exact fp32 dot; fine = 0: the lowest plane is
+// all zero), then planes 3 (the top digits), 2, 1 and 0, 32 signed bytes each.
 constexpr int kXqBytes = kXqBlockBytes;
-static_assert(kXqBytes == 16 + 3 * 32, "header + three planes");
+constexpr int kXqHeader = 32;
+static_assert(kXqBytes == kXqHeader + 4 * 32, "header + four planes");
 
 template <int FMT, bool PL = false>
 struct StreamLayout {
@@ -166,7 +179,9 @@ struct StreamLayout {
     static constexpr int CHUNK_BYTES = (C::BPC * C::VPB + 1) * kVecBytes;  // one group's chunk
     static constexpr int XE = C::BPC * C::E;                           // x elements of a unit
     static constexpr int GPU = kStreamWarps * C::GPW;                  // row groups of a unit
-    static constexpr int SLOT_BYTES = GPU * CHUNK_BYTES + XE * 4;  // planes take less than fp32
+    // x of a unit: fp32, or its planes (5 bytes per element)
+    static constexpr int XBYTES = XE * 4 > XE / 32 * kXqBytes ? XE * 4 : XE / 32 * kXqBytes;
+    static constexpr int SLOT_BYTES = GPU * CHUNK_BYTES + XBYTES;
     // shared memory: [full S][empty S][abort][info S][ring S*SLOT]; info:
     // which unit a slot holds when units are taken at run time
     static constexpr int OFF_FULL = 0;
@@ -267,35 +282,80 @@ __device__ __forceinline__ int plane_pos(int l) {
     if (FMT == Q4_0) return 4 * (2 * (l >> 3) + (l & 1)) + ((l & 7) >> 1);
     return l;
 }
-// The warp converts one block of 32 elements of x into its planes at dst;
-// lane l holds element l in v.
+// x blocks (of 32 elements) in one chunk of the stream kernel: xprep_kernel
+// gives all x blocks of a chunk one grid tier, so that a consumer branches
+// once per chunk.
 template <int FMT>
-__device__ __forceinline__ void x_block_to_planes(float v, uint8_t *dst, int lane) {
-    constexpr int OFF = FMT == Q4_0 ? 8 : 128;
+constexpr int xq_chunk_blocks() { return StreamCfg<FMT>::BPC * StreamCfg<FMT>::E / 32; }
+
+// One 32-element block of x rounded to integers (the warp works on one block;
+// lane l holds element l in v).
+//   The fine grid: t = v * 2^sf, sf = 30 - floor(log2(max |v|)), so the
+//   block's largest |t| lies in [2^30, 2^31) and X = round(t) fits int32 (sf is
+//   capped at 122 for blocks of tiny values: 2^-(sf+4) stays a normal float).
+//   The coarse grid is 256 times wider (t / 256, |.| < 2^23).  t, t / 256 and
+//   their rounding residues are exact in fp32.  An element is held precisely
+//   enough when its residue is at most 2^-14 of itself.
+//   tier 0: every element is, on the coarse grid: X = 256 * round(t / 256)
+//           (clamped to 2^23 - 1 before the product), lowest byte zero;
+//   tier 1: every element is on the fine grid: X = round(t);
+//   tier 2: not even that (a small value next to an outlier channel), or an
+//           Inf or NaN in the block: the consumers take the exact fp32 dot.
+struct XBlock {
+    int X;     // this lane's integer
+    int sf;    // fine-grid exponent
+    int tier;  // 0, 1, 2 (warp-uniform)
+};
+__device__ __forceinline__ XBlock x_block_quantize(float v) {
     const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
-    // |x| * 2^s <= 2^22 for the block's largest |x| (s capped for tiny blocks)
-    const int s = min(21 - ((int)(mx >> 23) - 127), 126);
-    const int X = __float2int_rn(v * __int_as_float((127 + s) << 23));
-    const int x0 = X & 255, x1 = (X >> 8) & 255, x2 = X >> 16;
-    const int pos = plane_pos<FMT>(lane);
-    dst[16 + pos] = (uint8_t)x2;
-    dst[48 + pos] = (uint8_t)x1;
-    dst[80 + pos] = (uint8_t)x0;
-    const int s2 = __reduce_add_sync(0xffffffffu, x2);
-    const int s1 = __reduce_add_sync(0xffffffffu, x1);
-    const int s0 = __reduce_add_sync(0xffffffffu, x0);
+    const int e = (int)(mx >> 23) - 127;  // floor(log2 max|v|); -127 for zero / subnormal
+    XBlock r;
+    r.sf = min(30 - e, 122);
+    const float tf = v * __int_as_float((127 + r.sf) << 23);  // exact
+    const float tc = tf * (1.f / 256.f);                      // exact
+    const float rc = rintf(tc), rf = rintf(tf);
+    // residues within 2^-14 of the element (true for t = 0, whose residue is 0)
+    const bool coarse_ok = fabsf(tc - rc) * 16384.f <= fabsf(tc);
+    const bool fine_ok = fabsf(tf - rf) * 16384.f <= fabsf(tf);
+    if (mx >= 0x7f800000u) r.tier = 2;
+    else if (__all_sync(0xffffffffu, coarse_ok)) r.tier = 0;
+    else r.tier = __all_sync(0xffffffffu, fine_ok) ? 1 : 2;
+    r.X = r.tier == 0 ? __float2int_rn(fminf(rc, 8388607.f)) * 256
+          : r.tier == 1 ? __float2int_rn(rf) : 0;
+    return r;
+}
+// Writes the block's planes at dst: the bytes of X, X = X3*2^24 + X2*2^16 +
+// X1*2^8 + X0 with X3 signed and the others in 0..255, each plane's header
+// init -128 * (its byte sum), the block's scale and the chunk's tier `mode`.
+template <int FMT>
+__device__ __forceinline__ void x_block_store(const XBlock &xb, int mode, uint8_t *dst, int lane) {
+    const int d0 = xb.X & 255, d1 = (xb.X >> 8) & 255, d2 = (xb.X >> 16) & 255, d3 = xb.X >> 24;
+    const int pos = kXqHeader + plane_pos<FMT>(lane);
+    dst[pos] = (uint8_t)d3;
+    dst[pos + 32] = (uint8_t)d2;
+    dst[pos + 64] = (uint8_t)d1;
+    dst[pos + 96] = (uint8_t)d0;
+    const int s3 = __reduce_add_sync(0xffffffffu, d3);
+    const int s2 = __reduce_add_sync(0xffffffffu, d2);
+    const int s1 = __reduce_add_sync(0xffffffffu, d1);
+    const int s0 = __reduce_add_sync(0xffffffffu, d0);
     if (lane == 0) {
-        // a block holding Inf or NaN gives NaN
-        const float inv =
-            mx >= 0x7f800000u ? __int_as_float(0x7fc00000) : __int_as_float((127 - s) << 23);
-        *reinterpret_cast<int4 *>(dst) = make_int4(-OFF * s2, -OFF * s1, -OFF * s0, __float_as_int(inv));
+        // Q4_0's dp4a sums come out 16 times the integer sum (nibbles read in
+        // place as 16 * q): its scale carries the 1/16
+        const int sc = xb.sf + (FMT == Q4_0 ? 4 : 0);
+        const float scale = xb.tier == 2 ? -1.f : __int_as_float((127 - sc) << 23);
+        reinterpret_cast<int4 *>(dst)[0] = make_int4(-128 * s3, -128 * s2, -128 * s1, -128 * s0);
+        reinterpret_cast<int4 *>(dst)[1] = make_int4(__float_as_int(scale), mode, 0, 0);
     }
 }
 
-// x of several problems as planes: blockIdx.y = problem, each warp converts
-// kXprepBlocks consecutive blocks of 32 elements (their loads issued first).
-// xq + p.xq0 receives the problem's K/32 plane blocks.
-constexpr int kXprepBlocks = 4;
+// x of several problems as planes: blockIdx.y = problem; each warp converts
+// kXprepBlocks consecutive x blocks (their loads issued first), the CTA's 8
+// warps one run of whole chunks of the stream kernel; the blocks' tiers meet
+// in shared memory to give each chunk its tier.  xq + p.xq0 receives the
+// problem's K/32 plane blocks.
+constexpr int kXprepBlocks = 2;
+constexpr int kXprepCtaBlocks = 8 * kXprepBlocks;
 struct XprepProb {
     const float *x;
     int64_t xq0;
@@ -311,20 +371,35 @@ struct XprepArgs {
 };
 template <int FMT, int NP>
 __global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ XprepArgs<NP> a) {
+    constexpr int G = xq_chunk_blocks<FMT>();
+    static_assert(kXprepCtaBlocks % G == 0, "a CTA converts whole chunks");
+    __shared__ int tiers[kXprepCtaBlocks];
     pdl_launch_dependents();
     pdl_wait();  // x may come from the previous kernel on the stream
     const XprepProb &p = a.p[blockIdx.y];
-    const int lane = (int)(threadIdx.x & 31);
-    const int b0 = ((int)blockIdx.x * 8 + (int)(threadIdx.x >> 5)) * kXprepBlocks;
-    if (b0 >= p.nb) return;
+    const int lane = (int)(threadIdx.x & 31), warp = (int)(threadIdx.x >> 5);
+    const int cta0 = (int)blockIdx.x * kXprepCtaBlocks;
+    const int b0 = cta0 + warp * kXprepBlocks;
     float v[kXprepBlocks];
 #pragma unroll
     for (int u = 0; u < kXprepBlocks; ++u)
         v[u] = b0 + u < p.nb ? p.x[32 * (int64_t)(b0 + u) + lane] : 0.f;
+    XBlock xb[kXprepBlocks];
 #pragma unroll
-    for (int u = 0; u < kXprepBlocks; ++u)
-        if (b0 + u < p.nb)
-            x_block_to_planes<FMT>(v[u], a.xq + p.xq0 + (int64_t)(b0 + u) * kXqBytes, lane);
+    for (int u = 0; u < kXprepBlocks; ++u) {
+        xb[u] = x_block_quantize(v[u]);
+        if (lane == 0) tiers[warp * kXprepBlocks + u] = b0 + u < p.nb ? xb[u].tier : 0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kXprepBlocks; ++u) {
+        if (b0 + u >= p.nb) break;
+        const int c0 = (warp * kXprepBlocks + u) / G * G;  // the chunk's first block in the CTA
+        int mode = 0;
+#pragma unroll
+        for (int j = 0; j < G; ++j) mode = max(mode, tiers[c0 + j]);
+        x_block_store<FMT>(xb[u], mode, a.xq + p.xq0 + (int64_t)(b0 + u) * kXqBytes, lane);
+    }
 }
 
 __device__ __forceinline__ uint32_t dp4a_us(uint32_t a, uint32_t b, uint32_t c) {
@@ -337,39 +412,101 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
     asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-// sum over one x block of (q - offset) * x, times 2^s; q bytes in w[0..7]
-// (four per word, in the block's plane order)
+// Integer sum over one x block of the weight bytes times x, in the block's
+// plane order: w[0..7] hold four raw weight bytes each.  The even words start
+// their chains at 0 and the odd ones at the header's -128 * (plane byte sum);
+// LO16 scales the even chains by 16 (Q4_0: the even words hold the low
+// nibbles, the odd ones the high nibbles in place, i.e. 16 * q).  FINE: the
+// lowest plane may be nonzero (tier 1), else it is all zero and skipped.
+// Returns the block's exact sum of (weight byte - offset) * X (times 16 for
+// Q4_0), rounded once to fp32.
+template <bool LO16, bool FINE>
 __device__ __forceinline__ float plane_dot(const uint32_t (&w)[8], const uint8_t *xq) {
     const int4 h = *reinterpret_cast<const int4 *>(xq);
-    const uint4 a2 = *reinterpret_cast<const uint4 *>(xq + 16), b2 = *reinterpret_cast<const uint4 *>(xq + 32);
-    const uint4 a1 = *reinterpret_cast<const uint4 *>(xq + 48), b1 = *reinterpret_cast<const uint4 *>(xq + 64);
-    const uint4 a0 = *reinterpret_cast<const uint4 *>(xq + 80), b0 = *reinterpret_cast<const uint4 *>(xq + 96);
+    const uint4 *pl = reinterpret_cast<const uint4 *>(xq + kXqHeader);
+    const uint4 a3 = pl[0], b3 = pl[1], a2 = pl[2], b2 = pl[3], a1 = pl[4], b1 = pl[5];
+    const uint32_t P3[8] = {a3.x, a3.y, a3.z, a3.w, b3.x, b3.y, b3.z, b3.w};
     const uint32_t P2[8] = {a2.x, a2.y, a2.z, a2.w, b2.x, b2.y, b2.z, b2.w};
     const uint32_t P1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
-    const uint32_t P0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
-    // two independent chains per plane (even and odd words) for latency
-    uint32_t s2 = (uint32_t)h.x, s1 = (uint32_t)h.y, s0 = (uint32_t)h.z;
-    uint32_t t2 = 0, t1 = 0, t0 = 0;
+    uint32_t P0[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (FINE) {
+        const uint4 a0 = pl[6], b0 = pl[7];
+        P0[0] = a0.x; P0[1] = a0.y; P0[2] = a0.z; P0[3] = a0.w;
+        P0[4] = b0.x; P0[5] = b0.y; P0[6] = b0.z; P0[7] = b0.w;
+    }
+    uint32_t s3 = 0, s2 = 0, s1 = 0, s0 = 0;
+    uint32_t t3 = (uint32_t)h.x, t2 = (uint32_t)h.y, t1 = (uint32_t)h.z, t0 = (uint32_t)h.w;
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {
-        s2 = dp4a_us(w[i], P2[i], s2);
+        s3 = dp4a_us(w[i], P3[i], s3);
+        s2 = dp4a_uu(w[i], P2[i], s2);
         s1 = dp4a_uu(w[i], P1[i], s1);
-        s0 = dp4a_uu(w[i], P0[i], s0);
-        t2 = dp4a_us(w[i + 1], P2[i + 1], t2);
+        t3 = dp4a_us(w[i + 1], P3[i + 1], t3);
+        t2 = dp4a_uu(w[i + 1], P2[i + 1], t2);
         t1 = dp4a_uu(w[i + 1], P1[i + 1], t1);
-        t0 = dp4a_uu(w[i + 1], P0[i + 1], t0);
+        if (FINE) {
+            s0 = dp4a_uu(w[i], P0[i], s0);
+            t0 = dp4a_uu(w[i + 1], P0[i + 1], t0);
+        }
     }
-    s2 += t2;
-    s1 += t1;
-    s0 += t0;
-    const float T = fmaf((float)(int)s2, 65536.f, fmaf((float)(int)s1, 256.f, (float)(int)s0));
-    return __int_as_float(h.w) * T;
+    constexpr int L = LO16 ? 16 : 1;
+    const int u3 = (int)s3 * L + (int)t3, u2 = (int)s2 * L + (int)t2, u1 = (int)s1 * L + (int)t1;
+    const int u0 = FINE ? (int)s0 * L + (int)t0 : 0;
+    // |u| < 2^21, so both halves are exact in int32.  T = hi * 2^16 + lo is
+    // rewritten as hi' * 2^16 + lo' with lo' = lo mod 2^16 in 0..65535 (the
+    // carry moves into hi'): the FMA then rounds once, without cancellation,
+    // and needs no 64-bit conversion (which would run on the FP64 pipe).
+    const int hi = u3 * 256 + u2, lo = u1 * 256 + u0;
+    const int hi2 = hi + (lo >> 16), lo2 = lo & 0xFFFF;
+    return fmaf((float)hi2, 65536.f, (float)lo2);
+}
+// The exact fallback for a marked x block: sum over its 32 elements of the
+// weight (d * (q - offset), exact in fp32) times x, in fp32, x read from
+// global memory (16-byte aligned).  wa, wb: w[0..3], w[4..7] of plane_dot.
+// Not inlined: it is the rare path, kept out of the unrolled block loops.
+template <int FMT>
+__device__ __noinline__ float exact_block_dot(uint4 wa, uint4 wb, float d, const float *xg) {
+    const uint32_t w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    float r = 0.f;
+#pragma unroll 1
+    for (int l = 0; l < 32; l += 4) {
+        const float4 xv = *reinterpret_cast<const float4 *>(xg + l);
+        const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = l + j;
+            int q;
+            if (FMT == Q4_0) {  // element 8t+i: bits 4i..4i+3 of packed word t
+                const int t = e >> 3, i = e & 7;
+                const uint32_t word = (i & 1) ? (w[2 * t + 1] >> 4) : w[2 * t];
+                q = (int)((word >> (8 * (i >> 1))) & 15u) - 8;
+            } else {  // byte e, stored + 128
+                q = (int)((w[e >> 2] >> (8 * (e & 3))) & 255u) - 128;
+            }
+            r = fmaf(d * (float)q, xs[j], r);
+        }
+    }
+    return r;
+}
+// One x block times the weights' scale d: the planes' integer sum times
+// d * 2^-sf (the two scales first, so that only a result beyond the fp32
+// range can overflow).  MODE is the chunk's tier: 0 all blocks on the coarse
+// grid, 1 some on the fine grid, 2 some marked for the exact fp32 dot (this
+// block's own scale, -1 when marked, decides).
+template <int FMT, int MODE>
+__device__ __forceinline__ float x_block_dot(const uint32_t (&w)[8], float d, const uint8_t *xq,
+                                             const float *xg) {
+    const float scale = *reinterpret_cast<const float *>(xq + 16);
+    if (MODE == 2 && scale < 0.f)
+        return exact_block_dot<FMT>(make_uint4(w[0], w[1], w[2], w[3]),
+                                    make_uint4(w[4], w[5], w[6], w[7]), d, xg);
+    return (d * scale) * plane_dot<FMT == Q4_0, MODE != 0>(w, xq);
 }
 // One block with x as planes: this lane's row, block b of the step at ws, x
-// planes of the chunk at xq.
-template <int FMT>
-__device__ __forceinline__ float block_dot_q(const uint8_t *ws, const uint8_t *xq, int b, float d,
-                                             int lane) {
+// planes of the chunk at xq, fp32 x of the chunk at xg.
+template <int FMT, int MODE>
+__device__ __forceinline__ float block_dot_q(const uint8_t *ws, const uint8_t *xq, const float *xg,
+                                             int b, float d, int lane) {
     using C = StreamCfg<FMT>;
     if (FMT == Q4_0) {
         const uint4 v = *reinterpret_cast<const uint4 *>(ws + b * kVecBytes + lane * 16);
@@ -377,10 +514,10 @@ __device__ __forceinline__ float block_dot_q(const uint8_t *ws, const uint8_t *x
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             const uint32_t x = word_of(v, t);
-            w[2 * t] = x & 0x0F0F0F0Fu;
-            w[2 * t + 1] = (x >> 4) & 0x0F0F0F0Fu;
+            w[2 * t] = x & 0x0F0F0F0Fu;      // low nibbles: q
+            w[2 * t + 1] = x & 0xF0F0F0F0u;  // high nibbles in place: 16 * q
         }
-        return d * plane_dot(w, xq + b * kXqBytes);
+        return x_block_dot<FMT, MODE>(w, d, xq + b * kXqBytes, xg + b * 32);
     } else {  // Q8_0 (one x block) or I8_B64 (two): stored bytes q + 128
         float r = 0.f;
 #pragma unroll
@@ -388,10 +525,35 @@ __device__ __forceinline__ float block_dot_q(const uint8_t *ws, const uint8_t *x
             const uint4 va = *reinterpret_cast<const uint4 *>(ws + (b * C::VPB + 2 * h) * kVecBytes + lane * 16);
             const uint4 vb = *reinterpret_cast<const uint4 *>(ws + (b * C::VPB + 2 * h + 1) * kVecBytes + lane * 16);
             const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-            r += plane_dot(w, xq + (b * (C::E / 32) + h) * kXqBytes);
+            r += x_block_dot<FMT, MODE>(w, d, xq + (b * (C::E / 32) + h) * kXqBytes,
+                                        xg + b * C::E + 32 * h);
         }
-        return d * r;
+        return r;
     }
+}
+// The blocks of one chunk with x as planes, for one chunk tier MODE.
+template <int FMT, int MODE>
+__device__ __forceinline__ float planes_chunk(const uint8_t *ws, const uint8_t *xq, const float *xg,
+                                              const uint4 &sv, int nbc, int sub, int lane) {
+    using C = StreamCfg<FMT>;
+    // Fully unrolled bodies only where they pay (tier 0, and full chunks of
+    // tier 1): more copies of the block body overflow the instruction cache
+    float acc = 0.f;
+    if (MODE != 2 && nbc == C::BPC) {
+#pragma unroll
+        for (int i = 0; i < C::BPC; ++i)
+            acc += block_dot_q<FMT, MODE>(ws, xq, xg, i, scale_of(sv, sub * C::BPC + i), lane);
+    } else if (MODE == 0) {
+#pragma unroll
+        for (int i = 0; i < C::BPC; ++i)
+            if (i < nbc)
+                acc += block_dot_q<FMT, MODE>(ws, xq, xg, i, scale_of(sv, sub * C::BPC + i), lane);
+    } else {
+#pragma unroll 1
+        for (int i = 0; i < nbc; ++i)
+            acc += block_dot_q<FMT, MODE>(ws, xq, xg, i, scale_of(sv, sub * C::BPC + i), lane);
+    }
+    return acc;
 }
 
 // ---- per-format consumer work on one chunk held in shared memory ------------
@@ -472,25 +634,22 @@ __device__ __forceinline__ float block_dot(const uint8_t *ws, const float *xb, i
 
 // This lane's row: sum over the chunk's blocks of w * x.  ws: the group's
 // chunk (nbc blocks of quant vectors, then the step's scale vector); xs: the
-// chunk's x; sub: the chunk's place in its step (for the scale slots).
+// chunk's x in shared memory (fp32, or its planes); xg: the chunk's fp32 x in
+// global memory (read only for x blocks marked for the exact dot); sub: the
+// chunk's place in its step (for the scale slots).
 template <int FMT>
-__device__ __forceinline__ float consume_chunk(const uint8_t *ws, const float *xs, int nbc, int sub,
-                                               int lane, const Magic &mg, bool planes) {
+__device__ __forceinline__ float consume_chunk(const uint8_t *ws, const float *xs, const float *xg,
+                                               int nbc, int sub, int lane, const Magic &mg,
+                                               bool planes) {
     using C = StreamCfg<FMT>;
     const uint4 sv = *reinterpret_cast<const uint4 *>(ws + nbc * C::VPB * kVecBytes + lane * 16);
     float acc = 0.f;
     if (XPlanes<FMT>::on && planes) {
         const uint8_t *xq = reinterpret_cast<const uint8_t *>(xs);
-        if (nbc == C::BPC) {
-#pragma unroll
-            for (int i = 0; i < C::BPC; ++i)
-                acc += block_dot_q<FMT>(ws, xq, i, scale_of(sv, sub * C::BPC + i), lane);
-        } else {
-#pragma unroll
-            for (int i = 0; i < C::BPC; ++i)
-                if (i < nbc) acc += block_dot_q<FMT>(ws, xq, i, scale_of(sv, sub * C::BPC + i), lane);
-        }
-        return acc;
+        const int mode = *reinterpret_cast<const int *>(xq + 20);  // the chunk's tier
+        if (mode == 0) return planes_chunk<FMT, 0>(ws, xq, xg, sv, nbc, sub, lane);
+        if (mode == 1) return planes_chunk<FMT, 1>(ws, xq, xg, sv, nbc, sub, lane);
+        return planes_chunk<FMT, 2>(ws, xq, xg, sv, nbc, sub, lane);
     }
     if (nbc == C::BPC) {
 #pragma unroll
@@ -540,9 +699,9 @@ __device__ __forceinline__ void q4_block_rows(const uint8_t *ws, int stride, con
 // All of a warp's live groups (nlive of GPW) on one unit: groups sit
 // kStreamWarps chunks apart in the slot.
 template <int FMT>
-__device__ __forceinline__ void consume_rows(const uint8_t *ws, const float *xs, int nbc, int sub,
-                                             int nlive, int lane, const Magic &mg, bool planes,
-                                             float (&acc)[StreamCfg<FMT>::GPW]) {
+__device__ __forceinline__ void consume_rows(const uint8_t *ws, const float *xs, const float *xg,
+                                             int nbc, int sub, int nlive, int lane, const Magic &mg,
+                                             bool planes, float (&acc)[StreamCfg<FMT>::GPW]) {
     using C = StreamCfg<FMT>;
     using L = StreamLayout<FMT>;
     constexpr int stride = kStreamWarps * L::CHUNK_BYTES;
@@ -575,7 +734,8 @@ __device__ __forceinline__ void consume_rows(const uint8_t *ws, const float *xs,
     }
 #pragma unroll
     for (int r = 0; r < C::GPW; ++r)
-        if (r < nlive) acc[r] += consume_chunk<FMT>(ws + r * stride, xs, nbc, sub, lane, mg, planes);
+        if (r < nlive)
+            acc[r] += consume_chunk<FMT>(ws + r * stride, xs, xg, nbc, sub, lane, mg, planes);
 }
 
 template <int FMT, int NP, bool PL>
@@ -818,7 +978,8 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
             const uint8_t *ws = ring + sl * L::SLOT_BYTES + warp * L::CHUNK_BYTES;
             const float *xs =
                 reinterpret_cast<const float *>(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES);
-            consume_rows<FMT>(ws, xs, q.nbc, q.sub, nlive, lane, mg, planes, acc);
+            const float *xg = p.x + (int64_t)(q.s * 8 + q.sub * C::BPC) * C::E;
+            consume_rows<FMT>(ws, xs, xg, q.nbc, q.sub, nlive, lane, mg, planes, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sl]);  // the slot is free; the sums are in registers

@@ -52,8 +52,15 @@
  *   - Device calls are asynchronous on `stream` (a cudaStream_t passed as
  *     void*, NULL = the legacy default stream) and make no host read-back, so
  *     they may be captured into a CUDA graph.
- *   - Argument errors are detected on the host and returned before any launch.
- *     A failed launch returns LEAN_ERR_CUDA (cudaGetLastError is consumed).
+ *   - Argument errors are detected on the host and returned before any launch
+ *     (nothing is queued on the stream).  A failed launch returns LEAN_ERR_CUDA
+ *     (cudaGetLastError is consumed).
+ *   - Per-device facts (the SM count, the device addresses of the library's
+ *     error word and fixed workspace, raised shared-memory limits) are looked
+ *     up on a device's first use and cached by device ordinal.  The library
+ *     therefore assumes each device is used through its primary context (the
+ *     one the CUDA runtime and PyTorch use) and is not reset with
+ *     cudaDeviceReset while the library is loaded.
  */
 #ifndef LEAN_QMATMUL_H
 #define LEAN_QMATMUL_H
@@ -172,16 +179,23 @@ int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);
  * larger than the SM count.
  *   workspace        device, 256-byte aligned, >= lean_qmatmul_workspace_bytes
  *                    bytes.  M = 1: it must be zeroed once (cudaMemset) before
- *                    its first use; every call leaves its arrival counters
- *                    zeroed again (the rest is scratch).  For Q4_0, Q8_0 and
- *                    I8_B64 calls that stream at least 32 MiB of weights
- *                    (lean_qmatmul_batch of a whole decode step, say), a
- *                    first kernel also writes x there as integer
- *                    planes (a power-of-two scale per 32 elements, 22 bits
- *                    of the block's largest |x|) so that the dot products
- *                    run on dp4a; results then differ from the fp32-x path
- *                    by at most 2^-23 of each block's largest |x| times
- *                    sum |w| per block.
+ *                    its first use; every call that completes leaves its
+ *                    arrival counters zeroed again (the rest is scratch).
+ *                    After a call for which lean_device_error() reports a
+ *                    timeout, counters may be left set: zero the workspace
+ *                    again before its next use.  For Q4_0, Q8_0 and I8_B64
+ *                    calls that stream at least 32 MiB of weights
+ *                    (lean_qmatmul_batch of a whole decode step, say), or
+ *                    that pass LEAN_FLAG_X_PLANES, a first kernel also writes
+ *                    x there as integer planes (a power-of-two scale per 32
+ *                    elements, a grid of 2^-21 or, where needed, 2^-29 of the
+ *                    block's largest |x|) so that the dot products run on
+ *                    dp4a.  A block of x in which even the finer grid would
+ *                    move an element by more than 2^-14 of the element
+ *                    itself (a small value next to an outlier channel), or
+ *                    which holds an Inf or NaN, is marked and takes the exact
+ *                    fp32 dot instead: every product w*x errs by at most
+ *                    2^-14 * |w*x| before the fp32 sums, whatever x is.
  *                    M >= 16: any contents; a first kernel writes x there as
  *                    bf16 hi / lo operand tiles, once for all CTAs, which the
  *                    product then copies with TMA (the fast path for large M).

@@ -73,16 +73,16 @@ def test_workspace_sizes(lean):
 
 def test_m1_workspace_layout(lean):
     """M = 1 workspace: 2 MiB of stream-K partial sums (512 CTAs x 2 sides x
-    16 groups x 32 rows, fp32), then x as planes (112 bytes per 32 elements,
+    16 groups x 32 rows, fp32), then x as planes (160 bytes per 32 elements,
     integer formats), then one counter per 32-row group, plus the two counters
     of the run-time hand-out for a batch of two or more; each region rounded up
     to 256 bytes."""
     part = 512 * 2 * 16 * 32 * 4
     r = lambda b: (b + 255) // 256 * 256
-    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 1) == part + r(30 * 112) + r(30 * 4)
+    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 1) == part + r(30 * 160) + r(30 * 4)
     assert lean.lean_qmatmul_workspace_bytes(3, 1000, 512, 1) == part + r(32 * 4)  # Q6_K: fp32 x
     two = lean.make_problems([(None, None, None, 960, 960), (None, None, None, 320, 2560)])
-    assert lean.lean_batch_workspace_bytes(0, two) == part + r((30 + 80) * 112) + r((30 + 10 + 2) * 4)
+    assert lean.lean_batch_workspace_bytes(0, two) == part + r((30 + 80) * 160) + r((30 + 10 + 2) * 4)
     one = lean.make_problems([(None, None, None, 960, 960)])
     assert lean.lean_batch_workspace_bytes(0, one) == lean.lean_qmatmul_workspace_bytes(0, 960, 960, 1)
     bad = lean.make_problems([(None, None, None, 960, 961)])

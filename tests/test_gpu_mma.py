@@ -156,9 +156,10 @@ def test_mma_early_weights_chain(lean):
 
 @pytest.mark.parametrize("fmt", FMTS, ids=IDS)
 def test_mma_caller_workspace(lean, fmt):
-    """With a caller-owned workspace (which then holds the split x) the bits
-    equal those of a call that takes its scratch from the stream-ordered pool;
-    a workspace smaller than the query says is refused before any launch."""
+    """With a caller-owned workspace (which then holds the split x, written
+    once by its own kernel) the bits equal those of a call without one (where
+    every CTA splits its own x; the library allocates nothing); a workspace
+    smaller than the query says is refused before any launch."""
     torch = torch_cuda()
     be = syn.BLOCK_ELEMS[fmt]
     N, K, M = 300, (4 if fmt == syn.Q6_K else 40) * be, 100

@@ -57,3 +57,45 @@ def test_fixed_workspace_limits():
              st) == lean.LEAN_ERR_SHAPE
     assert f(9, buf.data_ptr(), buf.data_ptr(), buf.data_ptr(), 32, 32, 0, st) == lean.LEAN_ERR_FORMAT
     assert f(0, buf.data_ptr(), buf.data_ptr(), buf.data_ptr(), 32, 48, 0, st) == lean.LEAN_ERR_SHAPE
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["plain", "early_weights"])
+def test_fixed_workspace_in_captured_graph(flags):
+    """The use the entry point exists for: after one warm call on the device,
+    the call is recorded by stream capture (its counter clear and its kernel
+    both become graph nodes), and the graph replayed twice into NaN-filled y
+    gives the caller-workspace result and stays within the oracle's
+    tolerance.  A call the library rejects inside the capture queues nothing
+    and leaves the capture usable."""
+    torch = torch_cuda()
+    from block_quantized_weight_dot_gb300 import lean
+    fmt, N, K = syn.Q4_0, 2048, 11008
+    W, x = syn.make_problem(fmt, N, K, 1, seed=(41, flags))
+    Wd = lean.upload_packed(fmt, W, N, K)
+    xd = torch.from_numpy(x).cuda()
+    nb = lean.lean_qmatmul_workspace_bytes(fmt, N, K, 1)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    y_ws = torch.empty((1, N), device="cuda")
+    lean.lean_qmatmul_ws(fmt, Wd, xd, y_ws, N, K, 1, 0, ws, nb)
+    y = torch.full((1, N), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        lean.lean_qmatmul_fixed_ws(fmt, Wd, xd, y, N, K, flags, s)  # first call: set-up
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            bad = lean._lib.lean_qmatmul_fixed_ws(fmt, Wd.data_ptr(), xd.data_ptr(), y.data_ptr(),
+                                                  N, K + 1, flags, s.cuda_stream)
+            lean.lean_qmatmul_fixed_ws(fmt, Wd, xd, y, N, K, flags, s)
+    assert bad == lean.LEAN_ERR_SHAPE
+    y_ref, bound = oracle.qmatmul(fmt, W, x, N, K, threads=4)
+    for _ in range(2):
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        a = y.cpu().numpy().astype(np.float64)
+        check_close(a, y_ws.cpu().numpy().astype(np.float64), bound, "graph vs caller workspace")
+        check_close(a, y_ref, bound, "graph vs oracle")
+    assert lean.lean_device_error(True) == 0
