@@ -32,38 +32,86 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
     tmp = _LIB + ".tmp.%d" % os.getpid()
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-                    "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"], check=True)
+    _gcc(_SRC, tmp)
     os.replace(tmp, _LIB)
     return _LIB
+
+
+def _gcc(src: str, out: str) -> None:
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                    "-Wall", "-Wextra", "-o", out, src, "-lm"], check=True)
+
+
+def source() -> str:
+    """Text of lean_oracle.c (the tests plant mistakes in copies of it)."""
+    with open(_SRC) as f:
+        return f.read()
+
+
+def build_variant(src_text: str, out_path: str) -> str:
+    """Compile C source text (a modified copy of lean_oracle.c, for the tests
+    that check the pins catch planted mistakes) into the library out_path."""
+    c_path = str(out_path) + ".c"
+    with open(c_path, "w") as f:
+        f.write(src_text)
+    _gcc(c_path, str(out_path))
+    return str(out_path)
+
+
+def _configure(lib):
+    c_i64, c_int = ctypes.c_int64, ctypes.c_int
+    vp = ctypes.c_void_p
+    lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_fp16_to_double.restype = ctypes.c_double
+    lib.oracle_block_elems.argtypes = [c_int]
+    lib.oracle_block_elems.restype = c_int
+    lib.oracle_block_bytes.argtypes = [c_int]
+    lib.oracle_block_bytes.restype = c_int
+    lib.oracle_dequant.argtypes = [c_int, vp, c_i64, c_i64, vp]
+    lib.oracle_dequant.restype = c_int
+    lib.oracle_qmatmul.argtypes = [c_int, vp, vp, vp, vp, c_i64, c_i64, c_i64, c_int]
+    lib.oracle_qmatmul.restype = c_int
+    lib.oracle_qmatmul_pairs.argtypes = [c_int, vp, vp, c_i64, c_i64, c_i64, c_i64,
+                                         vp, vp, vp, vp]
+    lib.oracle_qmatmul_pairs.restype = c_int
+    lib.oracle_quantize.argtypes = [c_int, vp, vp, c_i64, c_i64]
+    lib.oracle_quantize.restype = c_int
+    lib.oracle_double_to_fp16.argtypes = [ctypes.c_double]
+    lib.oracle_double_to_fp16.restype = c_int
+    return lib
+
+
+def load_library(path: str):
+    """A ctypes handle on an oracle library built from (a copy of) lean_oracle.c."""
+    return _configure(ctypes.CDLL(str(path)))
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            c_i64, c_int = ctypes.c_int64, ctypes.c_int
-            vp = ctypes.c_void_p
-            lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
-            lib.oracle_fp16_to_double.restype = ctypes.c_double
-            lib.oracle_block_elems.argtypes = [c_int]
-            lib.oracle_block_elems.restype = c_int
-            lib.oracle_block_bytes.argtypes = [c_int]
-            lib.oracle_block_bytes.restype = c_int
-            lib.oracle_dequant.argtypes = [c_int, vp, c_i64, c_i64, vp]
-            lib.oracle_dequant.restype = c_int
-            lib.oracle_qmatmul.argtypes = [c_int, vp, vp, vp, vp, c_i64, c_i64, c_i64, c_int]
-            lib.oracle_qmatmul.restype = c_int
-            lib.oracle_qmatmul_pairs.argtypes = [c_int, vp, vp, c_i64, c_i64, c_i64, c_i64,
-                                                 vp, vp, vp, vp]
-            lib.oracle_qmatmul_pairs.restype = c_int
-            lib.oracle_quantize.argtypes = [c_int, vp, vp, c_i64, c_i64]
-            lib.oracle_quantize.restype = c_int
-            lib.oracle_double_to_fp16.argtypes = [ctypes.c_double]
-            lib.oracle_double_to_fp16.restype = c_int
-            _lib = lib
+            _lib = load_library(build())
     return _lib
+
+
+class using:
+    """Context manager: route this module's functions to another oracle
+    library (load_library) for the duration of the block."""
+
+    def __init__(self, lib):
+        self.lib = lib
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self.saved = _lib
+        _lib = self.lib
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
 
 
 def _ptr(a: np.ndarray):
