@@ -6,9 +6,13 @@ q/k/v/o/gate/up/down, M=1, a fresh seeded x per linear), i.e. 224 GEMVs and
 weights already resident in HBM; steps alternate between weight copies whose
 total exceeds twice the L2, so every step streams its weights from HBM.
 
-Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
-on the host cores instead.  `--sweep` also prints one line per workload for
-the other shapes (to stderr), which the default run does not.
+Prints one JSON line (rank 0).  At one GPU the line also carries the same
+decode step with each layer's dependencies kept (per layer [q,k,v] -> o ->
+[gate,up] -> down, 128 calls) and a `per_config` list timing every other
+workload one product at a time (the 960x960 GEMV, TinyLlama Q8_0 / INT8-B64,
+the Qwen2.5-3B FFN at M = 1..256, the Q6_K lm_head).  `--impl reference`
+times the fp64 CPU oracle on the host cores instead.  `--sweep` prints the
+per-workload timings to stderr as well.
 """
 from __future__ import annotations
 
@@ -32,6 +36,9 @@ from block_quantized_weight_dot_gb300 import synthetic as syn  # noqa: E402
 
 METRIC = ("Q4_0 GEMV achieved HBM GB/s (% of GB300 peak) and decode-step linears/s, M=1")
 HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+# a GPU sleep of about 1 ms (at ~2 GHz) ahead of each timed region
+HEAD_START_CYCLES = 2_000_000
 
 
 # ---------------------------------------------------------------- helpers ---
@@ -70,6 +77,16 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return HBM_FALLBACK_GBS, "fallback"
+
+
+def measured_bf16():
+    """Dense bf16 TFLOP/s measured on this machine (burst: a kernel timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return BF16_FALLBACK_TFLOPS, "fallback"
 
 
 def kernel_source_hash():
@@ -324,6 +341,10 @@ def time_gpu(args, wl):
     barrier()
     torch.cuda.synchronize()
     t0 = time.time()
+    with torch.cuda.stream(stream):
+        # keep the GPU busy while the host enqueues the timed steps, so that
+        # host launch latency does not fall inside the timed region
+        torch.cuda._sleep(HEAD_START_CYCLES)
     ev0.record(stream)
     with torch.cuda.stream(stream):
         for s in range(args.steps):
@@ -361,6 +382,8 @@ def time_gpu(args, wl):
             e2e_step(s)
     torch.cuda.synchronize()
     barrier()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HEAD_START_CYCLES)
     e0.record(stream)
     with torch.cuda.stream(stream):
         for s in range(e_steps):
@@ -462,6 +485,8 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="also time every workload (stderr)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload timings and the layer-order decode step")
     ap.add_argument("--quantize", action="store_true",
                     help="time the host quantizer lean_quantize instead (no GPU)")
     args = ap.parse_args()
@@ -523,7 +548,17 @@ def main():
     config.update({"l2_defeat": "weights rotate over %d copies (%.0f MB > 2x L2 of %.0f MB)"
                    % (r["copies"], r["copies"] * wl.weight_bytes / 1e6, r["l2"] / 1e6),
                    "graph": "one CUDA graph per weight copy; a step = one graph replay",
+                   "timing": "CUDA events on the launching stream; a ~1 ms GPU sleep precedes "
+                             "the first event so the host has enqueued the timed steps",
                    "parallelism": "replicas" if ws > 1 else "single GPU"})
+    per_config = dependent = None
+    if ws == 1 and not args.no_per_config and args.workload == "decode_stack":
+        import torch
+        device = torch.device("cuda", local)
+        stream = torch.cuda.Stream(device)
+        dependent = time_dependent_step(device, r["l2"], stream, min(args.steps, 200),
+                                        max(3, min(args.warmup, 20)))
+        per_config = time_per_config(device, r["l2"], stream)
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True,
@@ -552,6 +587,11 @@ def main():
         "gpu_launches": r["launches"] * args.steps,
         "clocks": r["clocks"],
         "spot_check_vs_oracle": r["spot_ok"],
+        # the same decode step with each layer's dependencies kept (128 calls)
+        "decode_step_layer_order": dependent,
+        # every other workload, one product at a time (CUDA events, weights
+        # rotating beyond L2); frac against the measured HBM peak
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
 
@@ -559,50 +599,163 @@ def main():
         sweep(args)
 
 
-def sweep(args):
-    """Per-linear timings: one CUDA graph holding one call per weight copy,
-    the copies together larger than 2.2x L2, so every call streams from HBM."""
+def linear_path(lin, tc_min):
+    if lin.M == 1:
+        return "stream"
+    return "simt" if lin.M < tc_min else "mma"
+
+
+def mma_issued_flops(lin):
+    """bf16 MMA work the tensor-core kernel issues for one product: three MMAs
+    (w_hi x_hi, w_hi x_lo, w_lo x_hi) per 16-wide K step for every 128-row
+    weight tile against the tile's rows of x padded to 16, K padded to 64."""
+    kp = -(-lin.K // 64) * 64
+    tiles = -(-lin.N // 128)
+    mp = 0
+    for m0 in range(0, lin.M, 256):
+        mp += -(-min(256, lin.M - m0) // 16) * 16
+    return 3 * 2 * 128 * tiles * mp * kp
+
+
+def time_linear(lin, device, l2, stream, reps=20):
+    """One product timed alone: a CUDA graph of one call per weight copy (the
+    copies together larger than 2.2x L2, so every call streams from HBM)."""
     import torch
+    peak, peak_kind = measured_peaks()
+    bf16_peak, bf16_kind = measured_bf16()
+    one = syn.Workload(lin.name, (lin,))
+    dw = DeviceWorkload(one, device, l2)
+    with torch.cuda.stream(stream):
+        dw.run_step(0, stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for c in range(dw.copies):
+                dw.run_step(c, stream)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HEAD_START_CYCLES)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t = ev0.elapsed_time(ev1) / reps / dw.copies * 1e-3
+    gbs = lin.algorithmic_bytes / t / 1e9
+    path = linear_path(lin, dw.lean.lean_tensor_core_min_m())
+    r = {"linear": lin.name, "fmt": syn.FORMAT_NAMES[lin.fmt], "N": lin.N, "K": lin.K,
+         "M": lin.M, "path": path, "us": round(t * 1e6, 3), "GB/s": round(gbs, 1),
+         "frac": round(gbs / peak, 4), "useful_TFLOP/s": round(lin.flops / t / 1e12, 3),
+         "launches": dw.launches_per_step, "copies": dw.copies}
+    if path == "mma":
+        issued = mma_issued_flops(lin) / t / 1e12
+        r["tensor_pipe"] = {"issued_bf16_TFLOP/s": round(issued, 1),
+                            "frac_of_bf16_peak": round(issued / bf16_peak, 4),
+                            "peak": bf16_peak, "peak_source": bf16_kind,
+                            "basis": "bf16 MMA work the kernel issues (3 MMAs per 16-wide K "
+                                     "step, x rows padded to 16, K to 64) over CUDA-event time"}
+    del dw, g
+    torch.cuda.empty_cache()
+    return r
+
+
+PER_CONFIG = [("q4_0_gemv_960x960", "gemv_960"), ("tinyllama_1.1b_q8_0", "tinyllama_q8_0"),
+              ("tinyllama_1.1b_i8_b64", "tinyllama_i8_b64")] + \
+             [("qwen2.5_3b_ffn_q4_0_M%d" % M, "qwen_ffn_M%d" % M) for M in syn.QWEN25_3B_FFN_BATCHES] + \
+             [("qwen2.5_3b_lm_head_q6_k", "lm_head_q6_k")]
+
+
+def time_per_config(device, l2, stream):
+    """Every other workload, one product at a time (each a list entry)."""
+    out = []
+    for cfg, name in PER_CONFIG:
+        for lin in workload_by_name(name).linears:
+            r = time_linear(lin, device, l2, stream)
+            r["config"] = cfg
+            out.append(r)
+    return out
+
+
+def time_dependent_step(device, l2, stream, steps, warmup):
+    """The SmolLM2-360M decode step with the dependencies of a real layer kept:
+    per layer [q, k, v] (one batch call) -> o -> [gate, up] (one batch call)
+    -> down, 128 calls per step in stream order with programmatic dependent
+    launch, one CUDA graph per weight copy (the copies larger than 2x L2)."""
+    import torch
+    from block_quantized_weight_dot_gb300 import lean
+    wl = syn.smollm2_360m_decode_stack()
+    dw = DeviceWorkload(wl, device, l2)
+    lins = dw.lins
+    groups = [[0, 1, 2], [3], [4, 5], [6]]
+    flags = lean.LEAN_FLAG_EARLY_WEIGHTS
+
+    def calls(c):
+        out = []
+        for layer in range(len(lins) // 7):
+            for grp in groups:
+                idx = [7 * layer + j for j in grp]
+                out.append(lean.make_problems(
+                    [(dw.W[c][i], dw.x.data_ptr() + 4 * dw.x_off[i],
+                      dw.y.data_ptr() + 4 * dw.y_off[i], lins[i].N, lins[i].K) for i in idx]))
+        return out
+
+    plan = [calls(c) for c in range(dw.copies)]
+    wsb = max(lean.lean_batch_workspace_bytes(lins[0].fmt, p) for p in plan[0])
+    ws = torch.zeros(max(256, wsb), dtype=torch.uint8, device=device)
+
+    def step(c):
+        for probs in plan[c]:
+            lean.lean_qmatmul_batch(lins[0].fmt, probs, flags, ws, wsb, stream)
+
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    graphs = []
+    for c in range(dw.copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                step(c)
+        graphs.append(g)
+    for s in range(warmup):
+        graphs[s % dw.copies].replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HEAD_START_CYCLES)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for s in range(steps):
+            graphs[s % dw.copies].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
     peak, _ = measured_peaks()
-    names = ["gemv_960", "tinyllama_q8_0", "tinyllama_i8_b64", "lm_head_q6_k"] + \
-            ["qwen_ffn_M%d" % M for M in syn.QWEN25_3B_FFN_BATCHES]
+    gbs = wl.algorithmic_bytes / (ms * 1e-3) / 1e9
+    calls_per_step = len(plan[0])
+    del dw, graphs
+    torch.cuda.empty_cache()
+    return {"workload": wl.name + "_layer_order",
+            "order": "per layer: [q,k,v] batch -> o -> [gate,up] batch -> down (stream order, "
+                     "programmatic dependent launch)",
+            "calls_per_step": calls_per_step, "launches_per_step": calls_per_step,
+            "ms_per_step": ms, "GB/s": gbs, "frac": gbs / peak,
+            "linears_per_s": len(lins) / (ms * 1e-3), "steps": steps, "warmup": warmup}
+
+
+def sweep(args):
+    """--sweep: every other workload, one line per product on stderr."""
+    import torch
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     stream = torch.cuda.Stream()
-    for name in names:
-        wl = workload_by_name(name)
-        for lin in wl.linears:
-            one = syn.Workload(lin.name, (lin,))
-            dw = DeviceWorkload(one, torch.device("cuda"), l2)
-            with torch.cuda.stream(stream):
-                dw.run_step(0, stream)
-            stream.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                with torch.cuda.graph(g, stream=stream):
-                    for c in range(dw.copies):
-                        dw.run_step(c, stream)
-            for i in range(3):
-                g.replay()
-            torch.cuda.synchronize()
-            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            n = 20
-            ev0.record(stream)
-            with torch.cuda.stream(stream):
-                for i in range(n):
-                    g.replay()
-            ev1.record(stream)
-            torch.cuda.synchronize()
-            t = ev0.elapsed_time(ev1) / n / dw.copies * 1e-3
-            gbs = lin.algorithmic_bytes / t / 1e9
-            print(json.dumps({"sweep": name, "linear": lin.name, "fmt": syn.FORMAT_NAMES[lin.fmt],
-                              "N": lin.N, "K": lin.K, "M": lin.M, "us": round(t * 1e6, 3),
-                              "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                              "TFLOP/s": round(lin.flops / t / 1e12, 3),
-                              "launches": dw.launches_per_step, "copies": dw.copies}),
-                  file=sys.stderr, flush=True)
-            del dw, g
-            torch.cuda.empty_cache()
+    for r in time_per_config(torch.device("cuda"), l2, stream):
+        print(json.dumps(dict(sweep=r.pop("config"), **r)), file=sys.stderr, flush=True)
 
 
 if __name__ == "__main__":

@@ -53,6 +53,9 @@ lean_status simt_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, 
 template <int FMT>
 lean_status dequant_fmt(const Geom &g, const uint8_t *W, float *w, cudaStream_t stream);
 template <int FMT>
+lean_status embed_fmt(const Geom &g, const uint8_t *W, const int32_t *ids, int64_t n_ids,
+                      float *out, unsigned *err, cudaStream_t stream);
+template <int FMT>
 lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
                     unsigned flags, void *ws, int64_t ws_bytes, unsigned *err,
                     cudaStream_t stream);

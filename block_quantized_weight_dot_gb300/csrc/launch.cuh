@@ -184,6 +184,17 @@ lean_status dequant_fmt(const Geom &g, const uint8_t *W, float *w, cudaStream_t 
     return cudaGetLastError() == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
 }
 
+template <int FMT>
+lean_status embed_fmt(const Geom &g, const uint8_t *W, const int32_t *ids, int64_t n_ids,
+                      float *out, unsigned *err, cudaStream_t stream) {
+    SimtArgs a = simt_args(g, W, nullptr, nullptr, 0);
+    const int64_t items = n_ids * g.blocks;  // one thread each
+    const int64_t blocks = (items + 255) / 256;
+    if (blocks > INT32_MAX) return LEAN_ERR_SHAPE;
+    embed_kernel<FMT><<<(unsigned)blocks, 256, 0, stream>>>(a, ids, n_ids, out, err);
+    return cudaGetLastError() == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
+}
+
 // --------------------------------------------------------- tensor-core path ---
 
 // K split of the tensor-core product: the cluster size that minimises
@@ -484,6 +495,8 @@ lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int6
     template lean_status simt_fmt<FMT>(const Geom &, const uint8_t *, const float *, float *,  \
                                        int64_t, unsigned, cudaStream_t);                       \
     template lean_status dequant_fmt<FMT>(const Geom &, const uint8_t *, float *, cudaStream_t); \
+    template lean_status embed_fmt<FMT>(const Geom &, const uint8_t *, const int32_t *, int64_t, \
+                                        float *, unsigned *, cudaStream_t);                    \
     template lean_status stream_fmt<FMT>(const HostProb *, int, unsigned, void *, int64_t,     \
                                          bool, unsigned *, cudaStream_t);                      \
     template lean_status mma_fmt<FMT>(const Geom &, const uint8_t *, const float *, float *,   \

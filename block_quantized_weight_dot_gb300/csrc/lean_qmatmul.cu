@@ -213,6 +213,29 @@ lean_status lean_dequant(int fmt, const void *W_packed_dev, float *w_dev, int64_
     return LEAN_ERR_FORMAT;
 }
 
+lean_status lean_embed_rows(int fmt, const void *W_packed_dev, const int32_t *ids_dev,
+                            float *out_dev, int64_t n_ids, int64_t N, int64_t K, void *stream) {
+    if (block_elems(fmt) == 0) return LEAN_ERR_FORMAT;
+    Geom g;
+    if (n_ids <= 0 || !make_geom(fmt, N, K, &g)) return LEAN_ERR_SHAPE;
+    if (n_ids > ((int64_t)1 << 40) / K) return LEAN_ERR_SHAPE;
+    if (!W_packed_dev || !ids_dev || !out_dev) return LEAN_ERR_NULL;
+    if (!aligned(W_packed_dev, 16) || !aligned(ids_dev, 4) || !aligned(out_dev, 16))
+        return LEAN_ERR_ALIGN;
+    unsigned *err = error_word();
+    if (!err) return LEAN_ERR_CUDA;
+    cudaGetLastError();
+    const uint8_t *W = (const uint8_t *)W_packed_dev;
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (fmt) {
+    case LEAN_Q4_0: return embed_fmt<Q4_0>(g, W, ids_dev, n_ids, out_dev, err, s);
+    case LEAN_Q8_0: return embed_fmt<Q8_0>(g, W, ids_dev, n_ids, out_dev, err, s);
+    case LEAN_I8_B64: return embed_fmt<I8_B64>(g, W, ids_dev, n_ids, out_dev, err, s);
+    case LEAN_Q6_K: return embed_fmt<Q6_K>(g, W, ids_dev, n_ids, out_dev, err, s);
+    }
+    return LEAN_ERR_FORMAT;
+}
+
 lean_status lean_wait_selftest(unsigned limit_us, void *stream) {
     if (limit_us < 1 || limit_us > 1000000) return LEAN_ERR_SHAPE;
     unsigned *err = error_word();

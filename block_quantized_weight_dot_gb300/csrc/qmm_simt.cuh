@@ -232,24 +232,16 @@ __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
 }
 
 // ---- dequantisation: w[n][k] fp32; one warp per (row group, block) ----
+// The E weights of one block of one row, exact in fp32, to out (16-byte
+// aligned): the same decode the products use, then the scale.
 template <int FMT>
-__global__ void __launch_bounds__(256) dequant_kernel(const SimtArgs a, float *w) {
-    constexpr int E = BlockTraits<FMT>::E;
+__device__ __forceinline__ void store_block(const BlockFrag<FMT> &f, const Magic &mg, float *out) {
     constexpr int VPB = BlockTraits<FMT>::VPB;
-    const int lane = threadIdx.x & 31;
-    const int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int64_t g = item / a.blocks, c = item % a.blocks;
-    if (g >= a.groups) return;
-    BlockFrag<FMT> f;
-    load_block<FMT>(f, a, a.W + g * a.group_vecs * kVecBytes + lane * kVec, c);
-    const int64_t n = g * kRowsPerGroup + lane;
-    if (n >= a.N) return;
-    float *out = w + n * a.K + c * E;
     if (FMT == Q4_0) {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             f32x2 p[4];
-            q4_word(word_of(f.v[0], t), a.mg, p);
+            q4_word(word_of(f.v[0], t), mg, p);
             const float2 q0 = unpack2(p[0]), q1 = unpack2(p[1]), q2 = unpack2(p[2]),
                          q3 = unpack2(p[3]);
             float4 *o = reinterpret_cast<float4 *>(out + 8 * t);
@@ -262,7 +254,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const SimtArgs a, float *w
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 f32x2 p[2];
-                i8_word(word_of(f.v[j], t), a.mg, p);
+                i8_word(word_of(f.v[j], t), mg, p);
                 const float2 q0 = unpack2(p[0]), q1 = unpack2(p[1]);
                 *reinterpret_cast<float4 *>(out + 16 * j + 4 * t) =
                     make_float4(f.d * q0.x, f.d * q0.y, f.d * q1.x, f.d * q1.y);
@@ -275,8 +267,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(const SimtArgs a, float *w
             const int w0 = 3 * sub;
             f32x2 p[8];
             q6_group(word_of(f.v[w0 / 4], w0 % 4), word_of(f.v[(w0 + 1) / 4], (w0 + 1) % 4),
-                     word_of(f.v[(w0 + 2) / 4], (w0 + 2) % 4), a.mg, p);
-            const float dsc = f.d * i8_byte(word_of(scv, sub >> 2), sub & 3, a.mg);
+                     word_of(f.v[(w0 + 2) / 4], (w0 + 2) % 4), mg, p);
+            const float dsc = f.d * i8_byte(word_of(scv, sub >> 2), sub & 3, mg);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float2 q0 = unpack2(p[2 * j]), q1 = unpack2(p[2 * j + 1]);
@@ -285,6 +277,51 @@ __global__ void __launch_bounds__(256) dequant_kernel(const SimtArgs a, float *w
             }
         }
     }
+}
+
+// w[n][k] for the whole matrix: one warp per (row group, block), lane = row.
+template <int FMT>
+__global__ void __launch_bounds__(256) dequant_kernel(const SimtArgs a, float *w) {
+    constexpr int E = BlockTraits<FMT>::E;
+    const int lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t g = item / a.blocks, c = item % a.blocks;
+    if (g >= a.groups) return;
+    BlockFrag<FMT> f;
+    load_block<FMT>(f, a, a.W + g * a.group_vecs * kVecBytes + lane * kVec, c);
+    const int64_t n = g * kRowsPerGroup + lane;
+    if (n >= a.N) return;
+    store_block<FMT>(f, a.mg, w + n * a.K + c * E);
+}
+
+// Error bit of an embedding id outside 0..N-1.
+constexpr unsigned kErrEmbedId = 16u;
+
+// Selected rows of the matrix (an embedding lookup): out[i][k] = w[ids[i]][k],
+// one thread per (id, block), consecutive threads on consecutive blocks of
+// one id.  An id outside 0..N-1 gives a row of NaN and sets kErrEmbedId in
+// the device error word.
+template <int FMT>
+__global__ void __launch_bounds__(256) embed_kernel(const SimtArgs a, const int32_t *ids,
+                                                    int64_t n_ids, float *out, unsigned *err) {
+    constexpr int E = BlockTraits<FMT>::E;
+    const int64_t item = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (item >= n_ids * a.blocks) return;
+    const int64_t i = item / a.blocks, c = item % a.blocks;
+    const int64_t n = ids[i];
+    float *o = out + i * a.K + c * E;
+    if (n < 0 || n >= a.N) {
+        const float4 nan4 = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
+                                        __int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+#pragma unroll
+        for (int j = 0; j < E; j += 4) *reinterpret_cast<float4 *>(o + j) = nan4;
+        if (c == 0) atomicOr(err, kErrEmbedId);
+        return;
+    }
+    BlockFrag<FMT> f;
+    load_block<FMT>(f, a, a.W + (n / kRowsPerGroup) * a.group_vecs * kVecBytes + (n % kRowsPerGroup) * kVec,
+                    c);
+    store_block<FMT>(f, a.mg, o);
 }
 
 }  // namespace lean

@@ -32,6 +32,7 @@ SIGNATURES = {
     "lean_pack": (_int, [_int, _vp, _vp, _i64, _i64]),
     "lean_unpack_canonical": (_int, [_int, _vp, _vp, _i64, _i64]),
     "lean_dequant": (_int, [_int, _vp, _vp, _i64, _i64, _vp]),
+    "lean_embed_rows": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "lean_qmatmul": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "lean_qmatmul_ex": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp]),
     "lean_qmatmul_workspace_bytes": (_i64, [_int, _i64, _i64, _i64]),
@@ -159,6 +160,13 @@ def lean_unpack_canonical(fmt: int, packed, N: int, K: int) -> np.ndarray:
 def lean_dequant(fmt: int, W_packed_dev, w_dev, N: int, K: int, stream=None) -> None:
     _check("lean_dequant", _lib.lean_dequant(fmt, _addr(W_packed_dev), _addr(w_dev), N, K,
                                              _stream(stream)))
+
+
+def lean_embed_rows(fmt: int, W_packed_dev, ids_dev, out_dev, n_ids: int, N: int, K: int,
+                    stream=None) -> None:
+    """out[i][k] = w[ids[i]][k] (an embedding lookup); ids: int32 device tensor."""
+    _check("lean_embed_rows", _lib.lean_embed_rows(fmt, _addr(W_packed_dev), _addr(ids_dev),
+                                                   _addr(out_dev), n_ids, N, K, _stream(stream)))
 
 
 def lean_qmatmul(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,

@@ -122,6 +122,24 @@ lean_status lean_unpack_canonical(int fmt, const void *packed_host, void *canon_
 lean_status lean_dequant(int fmt, const void *W_packed_dev, float *w_dev,
                          int64_t N, int64_t K, void *stream);
 
+/* Embedding lookup: the listed rows of a quantized matrix as fp32.
+ * The "lean" README (model table) stores the embedding table as Q6_K, and
+ * the "oxinfer" crate page (Pre-quantized checkpoints) dequantizes a
+ * quantized embedding table one row per token; this is that step, for any of
+ * the four formats.  out_dev[i][k] = w[ids_dev[i]][k], bit for bit what
+ * lean_dequant gives for that row.
+ *   W_packed_dev  device, 16-byte aligned: the N x K table packed by lean_pack
+ *   ids_dev       device, 4-byte aligned, int32[n_ids], each in 0 .. N-1 (any
+ *                 order, repeats allowed); read only
+ *   out_dev       device, 16-byte aligned, float[n_ids][K], overwritten
+ * An id outside 0 .. N-1 cannot be reported by the call (it runs on the
+ * stream): its row of out_dev is filled with NaN and bit 16 of the device
+ * error word is set (lean_device_error).  Host-side errors as for the other
+ * calls: LEAN_ERR_FORMAT, LEAN_ERR_SHAPE (n_ids, N or K <= 0, K not a multiple
+ * of the block), LEAN_ERR_NULL, LEAN_ERR_ALIGN. */
+lean_status lean_embed_rows(int fmt, const void *W_packed_dev, const int32_t *ids_dev,
+                            float *out_dev, int64_t n_ids, int64_t N, int64_t K, void *stream);
+
 /* The product.  y[m][n] = sum_k w[n][k] * x[m][k], accumulated in fp32.
  *   W_packed_dev  device, 16-byte aligned, lean_packed_bytes(fmt,N,K) bytes
  *                 made by lean_pack (read only)
@@ -266,9 +284,10 @@ int64_t lean_fixed_workspace_bytes(void);
 
 /* The device error word of the current device: non-zero when a kernel gave up
  * waiting on one of its own pipeline barriers (a bounded wait timed out and
- * the kernel returned early; its outputs are then invalid).  Bits: 1 a stream
- * consumer waited too long for a slot, 2 a stream producer for a free slot,
- * 4 the tensor-core product for a stage, 8 lean_wait_selftest.  Reads it
+ * the kernel returned early; its outputs are then invalid) or met an index
+ * out of its range.  Bits: 1 a stream consumer waited too long for a slot, 2
+ * a stream producer for a free slot, 4 the tensor-core product for a stage, 8
+ * lean_wait_selftest, 16 lean_embed_rows was given an id outside 0 .. N-1.  Reads it
  * synchronously (the device is synchronised first) and clears it when
  * `clear` is non-zero.  Returns 0xFFFFFFFF if the word cannot be read. */
 unsigned lean_device_error(int clear);

@@ -18,6 +18,16 @@ def test_default_line_has_the_contract_fields(monkeypatch):
             "e2e_zero_copy": True, "e2e_same": True, "planes": True,
             "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}}
     monkeypatch.setattr(bench, "time_gpu", lambda args, wl: dict(fake))
+    per = [{"config": "q4_0_gemv_960x960", "linear": "gemv", "path": "stream", "us": 3.0,
+            "frac": 0.03},
+           {"config": "qwen2.5_3b_ffn_q4_0_M64", "linear": "l", "path": "mma", "us": 9.0,
+            "frac": 0.3, "tensor_pipe": {"frac_of_bf16_peak": 0.2}}]
+    dep = {"workload": "w", "ms_per_step": 0.2, "calls_per_step": 128, "frac": 0.13}
+    monkeypatch.setattr(bench, "time_per_config", lambda device, l2, stream: list(per))
+    monkeypatch.setattr(bench, "time_dependent_step",
+                        lambda device, l2, stream, steps, warmup: dict(dep))
+    import torch
+    monkeypatch.setattr(torch.cuda, "Stream", lambda device=None: None)
     monkeypatch.setattr(sys, "argv", ["bench.py", "--no-cpu-baseline", "--steps", "5",
                                       "--warmup", "3"])
     for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
@@ -41,3 +51,7 @@ def test_default_line_has_the_contract_fields(monkeypatch):
     assert e2e["h2d_bytes_per_step"] == 1064960 and e2e["d2h_bytes_per_step"] == 1105920
     assert e2e["matches_device_buffers"] is True
     assert line["config"]["workload"] == "smollm2_360m_q4_0_decode_stack_32L"
+    # every other workload and the layer-order decode step ride on the same line
+    assert [p["config"] for p in line["per_config"]] == [p["config"] for p in per]
+    assert line["per_config"][1]["tensor_pipe"]["frac_of_bf16_peak"] == 0.2
+    assert line["decode_step_layer_order"]["calls_per_step"] == 128
