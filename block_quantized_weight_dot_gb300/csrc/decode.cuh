@@ -16,6 +16,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include "layout.h"
 #include "ptx.cuh"
 
 namespace lean {
@@ -76,6 +77,28 @@ __device__ __forceinline__ Magic pin(const Magic &g) {
     m.i8 = pin64(g.i8);
 #pragma unroll
     for (int i = 0; i < 8; ++i) m.q6[i] = pin64(g.q6[i]);
+    return m;
+}
+
+// The same, for one format: only the constants its decoder uses are copied
+// (the others stay zero and are never read), which saves about twenty
+// registers in the Q4_0 and int8 kernels.
+template <int FMT>
+__device__ __forceinline__ Magic pin_fmt(const Magic &g) {
+    Magic m = {};
+    m.m0 = pin32(g.m0);  // every format (int8 sub-scales use it too)
+    if (FMT == Q4_0) {
+        m.m4 = pin32(g.m4); m.m8 = pin32(g.m8); m.m12 = pin32(g.m12); m.m16 = pin32(g.m16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m.q4[i] = pin64(g.q4[i]);
+    } else if (FMT == Q6_K) {
+        m.m6 = pin32(g.m6); m.m12 = pin32(g.m12); m.m14 = pin32(g.m14);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m.q6[i] = pin64(g.q6[i]);
+    } else {  // Q8_0, I8_B64
+        m.m8 = pin32(g.m8);
+        m.i8 = pin64(g.i8);
+    }
     return m;
 }
 

@@ -59,6 +59,9 @@ template <int FMT>
 lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
                     unsigned flags, void *ws, int64_t ws_bytes, unsigned *err,
                     cudaStream_t stream);
+// M = 1 on the one-wave kernel; *done = false when the problems do not fit it
+template <int FMT>
+lean_status gemv_fmt(const HostProb *ph, int n, unsigned flags, cudaStream_t stream, bool *done);
 // planes: with a workspace, hand x to the integer formats as planes (dp4a)
 template <int FMT>
 lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,

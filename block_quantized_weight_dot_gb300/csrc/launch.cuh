@@ -10,6 +10,7 @@
 #include "../../include/lean_qmatmul.h"
 #include "dispatch.h"
 #include "layout.h"
+#include "qmm_gemv.cuh"
 #include "qmm_mma.cuh"
 #include "qmm_simt.cuh"
 #include "qmm_stream.cuh"
@@ -294,6 +295,84 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
     return LEAN_OK;
 }
 
+// ------------------------------------------------------- one-wave M = 1 path ---
+
+// CTAs of qmm_gemv_kernel<FMT, NP> resident per SM (read once per device).
+template <int FMT, int NP>
+inline int gemv_ctas_per_sm() {
+    static std::atomic<int> cache[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        constexpr int smem = (kGemvWarps * GemvCfg<FMT>::NB * BlockTraits<FMT>::E + 256) * 4;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, qmm_gemv_kernel<FMT, NP>,
+                                                          kGemvThreads, smem) != cudaSuccess ||
+            v <= 0)
+            v = -1;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// The product on qmm_gemv_kernel when every problem fits it and the whole
+// grid fits the GPU at once; *done = false leaves the call to the stream path.
+template <int FMT, int NP>
+lean_status launch_gemv(const HostProb *ph, int n, unsigned flags, cudaStream_t stream,
+                        bool *done) {
+    constexpr int NB = GemvCfg<FMT>::NB;
+    *done = false;
+    // the smallest cluster for which every row's blocks fit 8 warps x NB
+    int64_t maxb = 0, groups = 0;
+    for (int i = 0; i < n; ++i) {
+        maxb = std::max<int64_t>(maxb, ph[i].g.blocks);
+        groups += ph[i].g.groups;
+    }
+    const int cl = (int)((maxb + kGemvWarps * NB - 1) / (kGemvWarps * NB));
+    if (cl > kGemvMaxCluster) return LEAN_OK;
+    const int per_sm = gemv_ctas_per_sm<FMT, NP>();
+    if (per_sm <= 0 || groups * cl > (int64_t)per_sm * sm_count()) return LEAN_OK;
+    GemvArgs<NP> a;
+    a.nprob = n;
+    a.cl = cl;
+    a.mg = make_magic();
+    int cta = 0;
+    for (int i = 0; i < n; ++i) {
+        const Geom &g = ph[i].g;
+        GemvProb &p = a.p[i];
+        p.W = ph[i].W;
+        p.x = ph[i].x;
+        p.y = ph[i].y;
+        p.N = (int)g.N;
+        p.K = (int)g.K;
+        p.blocks = (int)g.blocks;
+        p.steps = g.steps;
+        p.last_blocks = g.last_blocks;
+        p.step_vecs = g.step_vecs;
+        p.nbw = (int)((g.blocks + kGemvWarps * cl - 1) / (kGemvWarps * cl));
+        p.cta0 = cta;
+        p.group_vecs = g.group_vecs;
+        cta += (int)g.groups * cl;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cta, 1, 1);
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = (kGemvWarps * NB * BlockTraits<FMT>::E + 256) * 4;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    fill_launch(cfg, attr, cl, flags);
+    *done = true;
+    return cudaLaunchKernelEx(&cfg, qmm_gemv_kernel<FMT, NP>, a) == cudaSuccess ? LEAN_OK
+                                                                              : LEAN_ERR_CUDA;
+}
+
+template <int FMT>
+lean_status gemv_fmt(const HostProb *ph, int n, unsigned flags, cudaStream_t stream, bool *done) {
+    if (n == 1) return launch_gemv<FMT, 1>(ph, n, flags, stream, done);
+    if (n <= 8) return launch_gemv<FMT, 8>(ph, n, flags, stream, done);
+    return launch_gemv<FMT, kMaxBatch>(ph, n, flags, stream, done);
+}
+
 // -------------------------------------------------------------- stream path ---
 
 // Total row groups of a problem list; false when the list is too long.
@@ -499,6 +578,7 @@ lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int6
                                         float *, unsigned *, cudaStream_t);                    \
     template lean_status stream_fmt<FMT>(const HostProb *, int, unsigned, void *, int64_t,     \
                                          bool, unsigned *, cudaStream_t);                      \
+    template lean_status gemv_fmt<FMT>(const HostProb *, int, unsigned, cudaStream_t, bool *); \
     template lean_status mma_fmt<FMT>(const Geom &, const uint8_t *, const float *, float *,   \
                                       int64_t, unsigned, void *, int64_t, unsigned *,          \
                                       cudaStream_t);

@@ -70,6 +70,37 @@ lean_status dispatch_stream(int fmt, const HostProb *ph, int n, unsigned flags, 
     return LEAN_ERR_FORMAT;
 }
 
+// M = 1: the one-wave kernel when the problems fit it, unless the caller asks
+// for the streaming kernel or the call takes x as integer planes (with a
+// workspace, Q4_0 / Q8_0 / I8_B64, LEAN_FLAG_X_PLANES or >= 32 MiB of weights);
+// otherwise the streaming kernel.
+lean_status dispatch_m1(int fmt, const HostProb *ph, int n, unsigned flags, void *ws,
+                        int64_t wsb, cudaStream_t s) {
+    int64_t wbytes = 0, groups = 0, xqb = 0;
+    for (int i = 0; i < n; ++i) {
+        wbytes += ph[i].g.total;
+        groups += ph[i].g.groups;
+        xqb += xq_bytes(fmt, ph[i].g.K);
+    }
+    // a workspace smaller than the size query gives is refused whichever
+    // kernel runs
+    if (ws && wsb < workspace_layout(groups, xqb, n > 1).total) return LEAN_ERR_SHAPE;
+    const bool planes = ws && fmt != LEAN_Q6_K &&
+                        ((flags & LEAN_FLAG_X_PLANES) || wbytes >= kPlanesMinWeightBytes);
+    if (!(flags & LEAN_FLAG_STREAM) && !planes) {
+        bool done = false;
+        lean_status st = LEAN_OK;
+        switch (fmt) {
+        case LEAN_Q4_0: st = gemv_fmt<Q4_0>(ph, n, flags, s, &done); break;
+        case LEAN_Q8_0: st = gemv_fmt<Q8_0>(ph, n, flags, s, &done); break;
+        case LEAN_I8_B64: st = gemv_fmt<I8_B64>(ph, n, flags, s, &done); break;
+        case LEAN_Q6_K: st = gemv_fmt<Q6_K>(ph, n, flags, s, &done); break;
+        }
+        if (done || st != LEAN_OK) return st;
+    }
+    return dispatch_stream(fmt, ph, n, flags, ws, wsb, true, s);
+}
+
 lean_status check_product(int fmt, const void *W, const float *x, const float *y, int64_t N,
                           int64_t K, int64_t M, unsigned flags, Geom *g) {
     if (block_elems(fmt) == 0) return LEAN_ERR_FORMAT;
@@ -77,7 +108,8 @@ lean_status check_product(int fmt, const void *W, const float *x, const float *y
     if (M > ((int64_t)1 << 31) / std::max<int64_t>(K, N)) return LEAN_ERR_SHAPE;
     if (!W || !x || !y) return LEAN_ERR_NULL;
     if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return LEAN_ERR_ALIGN;
-    if (flags & ~(unsigned)(LEAN_FLAG_EARLY_WEIGHTS | LEAN_FLAG_X_PLANES)) return LEAN_ERR_FORMAT;
+    if (flags & ~(unsigned)(LEAN_FLAG_EARLY_WEIGHTS | LEAN_FLAG_X_PLANES | LEAN_FLAG_STREAM))
+        return LEAN_ERR_FORMAT;
     return LEAN_OK;
 }
 
@@ -118,7 +150,7 @@ lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_de
     cudaStream_t s = (cudaStream_t)stream;
     if (M == 1) {
         HostProb hp = {W, x_dev, y_dev, g};
-        return dispatch_stream(fmt, &hp, 1, flags, workspace, workspace_bytes, true, s);
+        return dispatch_m1(fmt, &hp, 1, flags, workspace, workspace_bytes, s);
     }
     if (M >= kMmaMinM) {
         unsigned *err = error_word();
@@ -190,8 +222,7 @@ lean_status lean_qmatmul_batch(int fmt, int count, const lean_problem *problems,
         hp[i].y = p.y;
     }
     cudaGetLastError();
-    return dispatch_stream(fmt, hp, count, flags, workspace, workspace_bytes, true,
-                           (cudaStream_t)stream);
+    return dispatch_m1(fmt, hp, count, flags, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 lean_status lean_dequant(int fmt, const void *W_packed_dev, float *w_dev, int64_t N, int64_t K,

@@ -1,0 +1,151 @@
+// qmm_gemv.cuh -- the M = 1 product for problems that fit the GPU in one
+// wave: latency first.
+//
+// A decode step is a chain of GEMVs in which each one's x is the previous
+// one's output ("wgpu-llm" README, Architecture at a Glance: N x (Attn + FFN)),
+// so what a single product costs after its input exists is what the step
+// pays.  This kernel takes every weight it needs off the critical path:
+//
+//  - a CTA of 8 warps owns one 32-row group (lane = row) and a range of its
+//    blocks along K; each warp takes at most NB consecutive blocks, and a
+//    cluster of up to 8 CTAs splits longer rows;
+//  - every lane loads all of its blocks (16-byte loads, 512 contiguous bytes
+//    per warp) before griddepcontrol.wait, so with programmatic dependent
+//    launch the weights stream while the previous kernel is still running;
+//  - after the wait the CTA stages its slice of x in shared memory (coalesced
+//    16-byte loads), each lane decodes its blocks exactly (decode.cuh) and
+//    sums w * x with paired fp32 FMAs, the warps' partial sums meet in shared
+//    memory and the cluster's in distributed shared memory, in a fixed order:
+//    no atomics, no workspace, deterministic.
+//
+// Several problems of one format can share a launch (a list of problems, each
+// owning a run of clusters), like the q, k and v projections of one layer.
+#pragma once
+#include <cooperative_groups.h>
+#include <stdint.h>
+
+#include "decode.cuh"
+#include "layout.h"
+#include "ptx.cuh"
+#include "qmm_simt.cuh"
+
+namespace lean {
+
+constexpr int kGemvWarps = 8;
+constexpr int kGemvThreads = 32 * kGemvWarps;
+constexpr int kGemvMaxCluster = 8;
+
+// Blocks a lane holds in registers at most (four 16-byte vectors per block of
+// the int8 formats: Q8_0 2, I8_B64 4; Q6_K 13 vectors).
+template <int FMT> struct GemvCfg;
+template <> struct GemvCfg<Q4_0> { static constexpr int NB = 8; };
+template <> struct GemvCfg<Q8_0> { static constexpr int NB = 4; };
+template <> struct GemvCfg<I8_B64> { static constexpr int NB = 2; };
+template <> struct GemvCfg<Q6_K> { static constexpr int NB = 1; };
+
+struct GemvProb {
+    const uint8_t *W;
+    const float *x;
+    float *y;
+    int N, K;
+    int blocks;      // blocks per row
+    int steps, last_blocks, step_vecs;
+    int nbw;         // blocks per warp (<= NB)
+    int cta0;        // first CTA of this problem (a multiple of the cluster size)
+    int64_t group_vecs;
+};
+
+template <int NP>
+struct GemvArgs {
+    int nprob;
+    int cl;  // CTAs per cluster (K split), the same for every problem
+    Magic mg;
+    GemvProb p[NP];
+};
+
+// vectors and scale of block c of this lane's row (as load_block, for a
+// GemvProb)
+template <int FMT>
+__device__ __forceinline__ void gemv_load(BlockFrag<FMT> &f, const GemvProb &p, const uint8_t *grp,
+                                          int c) {
+    constexpr int VPB = BlockTraits<FMT>::VPB;
+    const int s = c >> 3, i = c & 7;
+    const int nblk = s == p.steps - 1 ? p.last_blocks : 8;
+    const uint8_t *step = grp + (int64_t)s * p.step_vecs * kVecBytes;
+#pragma unroll
+    for (int j = 0; j < VPB; ++j)
+        f.v[j] = __ldg(reinterpret_cast<const uint4 *>(step + (i * VPB + j) * kVecBytes));
+    const unsigned short *sv = reinterpret_cast<const unsigned short *>(step + nblk * VPB * kVecBytes);
+    f.d = h2f(__ldg(sv + i));
+}
+
+// grid.x = sum over problems of groups * cl; cluster = (cl, 1, 1);
+// blockDim.x = 256; dynamic shared memory: the CTA's x slice (8 * nbw * E
+// floats of the largest problem) then 8 x 32 partial sums.
+template <int FMT, int NP>
+__global__ void __launch_bounds__(kGemvThreads, 3) qmm_gemv_kernel(const __grid_constant__ GemvArgs<NP> a) {
+    namespace cg = cooperative_groups;
+    constexpr int E = BlockTraits<FMT>::E;
+    constexpr int NB = GemvCfg<FMT>::NB;
+    extern __shared__ __align__(16) float gsm[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // this CTA's problem: the last one whose first CTA is at or before it
+    int lo = 0, hi = a.nprob - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.p[mid].cta0 <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    }
+    const int pi = lo;
+    const GemvProb &p = a.p[pi];
+    const int local = (int)blockIdx.x - p.cta0;
+    const int rank = local % a.cl;
+    const int64_t g = local / a.cl;
+    // blocks of this CTA and of this warp
+    const int span = kGemvWarps * p.nbw;
+    const int c0 = min(p.blocks, rank * span), c1 = min(p.blocks, c0 + span);
+    const int w0 = min(c1, c0 + warp * p.nbw), w1 = min(c1, w0 + p.nbw);
+    const uint8_t *grp = p.W + g * p.group_vecs * kVecBytes + lane * kVec;
+
+    pdl_launch_dependents();
+    BlockFrag<FMT> f[NB];
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+        if (w0 + i < w1) gemv_load<FMT>(f[i], p, grp, w0 + i);
+    const Magic mg = pin_fmt<FMT>(a.mg);
+    pdl_wait();  // x may come from the previous kernel on the stream
+
+    float *xs = gsm;
+    const float4 *src = reinterpret_cast<const float4 *>(p.x + (int64_t)c0 * E);
+    for (int i = threadIdx.x; i < (c1 - c0) * (E / 4); i += kGemvThreads)
+        reinterpret_cast<float4 *>(xs)[i] = src[i];
+    __syncthreads();
+
+    float tot[1] = {0.f};
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+        if (w0 + i < w1) block_fma<FMT, 1>(f[i], xs + (w0 + i - c0) * E, 0, mg, tot);
+
+    // the 8 warps' sums, then (cluster) the CTAs' sums, each in a fixed order
+    float *red = gsm + kGemvWarps * GemvCfg<FMT>::NB * E;
+    red[warp * 32 + lane] = tot[0];
+    __syncthreads();
+    const int64_t n = g * kRowsPerGroup + threadIdx.x;
+    if (threadIdx.x < 32) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kGemvWarps; ++w) s += red[w * 32 + threadIdx.x];
+        red[threadIdx.x] = s;
+        if (a.cl == 1 && n < p.N) p.y[n] = s;
+    }
+    if (a.cl == 1) return;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (rank == 0 && threadIdx.x < 32) {
+        float s = red[threadIdx.x];
+        for (int r = 1; r < a.cl; ++r) s += cluster.map_shared_rank(red, r)[threadIdx.x];
+        if (n < p.N) p.y[n] = s;
+    }
+    cluster.sync();  // no CTA leaves while rank 0 reads its shared memory
+}
+
+}  // namespace lean

@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
         }
     } else {
         // -------------------------------------------------------- converters
-        const Magic mg = pin(a.mg);
+        const Magic mg = pin_fmt<FMT>(a.mg);
         const int row = threadIdx.x & (kMmaRows - 1), half = threadIdx.x >> 7;
         const int g = row / kRowsPerGroup;
         const bool row_live = n0 / kRowsPerGroup + g < a.groups;

@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
     const uint8_t *grp = a.W + (g * a.group_vecs) * kVecBytes + lane * kVec;
 
     pdl_launch_dependents();
-    const Magic mg = pin(a.mg);
+    const Magic mg = pin_fmt<FMT>(a.mg);
     BlockFrag<FMT> fa, fb;
     if (w0 < w1) load_block<FMT>(fa, a, grp, w0);
     pdl_wait();  // x may come from the previous kernel on the stream

@@ -949,7 +949,7 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
     // published and finished by the last CTA to arrive.
     constexpr bool planes = PL && XPlanes<FMT>::on;
     Magic mg;  // decode constants, in registers only for the fp32-x variant
-    if constexpr (!planes) mg = pin(a.mg);
+    if constexpr (!planes) mg = pin_fmt<FMT>(a.mg);
     float acc[C::GPW];
 #pragma unroll
     for (int r = 0; r < C::GPW; ++r) acc[r] = 0.f;

@@ -21,6 +21,7 @@ LEAN_Q4_0, LEAN_Q8_0, LEAN_I8_B64, LEAN_Q6_K = 0, 1, 2, 3
 LEAN_OK, LEAN_ERR_FORMAT, LEAN_ERR_SHAPE, LEAN_ERR_NULL, LEAN_ERR_ALIGN, LEAN_ERR_CUDA = range(6)
 LEAN_FLAG_EARLY_WEIGHTS = 1
 LEAN_FLAG_X_PLANES = 2
+LEAN_FLAG_STREAM = 4
 
 # every symbol the header declares, with (restype, argtypes)
 _i64, _int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p

@@ -146,7 +146,10 @@ lean_status lean_embed_rows(int fmt, const void *W_packed_dev, const int32_t *id
  *   x_dev         device, 16-byte aligned, x[M][K] fp32 row-major (read only)
  *   y_dev         device, 4-byte aligned, y[M][N] fp32 row-major, overwritten
  *   stream        cudaStream_t as void*
- * M = 1 is the decode GEMV; M = 2..15 runs on the CUDA cores with each
+ * M = 1 is the decode GEMV: a product whose row groups fit the GPU in one
+ * wave runs on a kernel that loads all of its weights first and reduces on
+ * chip, a larger one streams its weights through a TMA ring; M = 2..15 runs on
+ * the CUDA cores with each
  * decoded weight reused M times; M >= 16 (lean_tensor_core_min_m()) runs on
  * the tcgen05 tensor cores
  * with split-bf16 operands (w = w_hi + w_lo, x = x_hi + x_lo, three MMAs into
@@ -170,7 +173,14 @@ enum {
     /* M = 1 with a workspace, Q4_0 / Q8_0 / I8_B64: always hand x to the
      * product as integer planes (dp4a), not only when the call streams at
      * least 32 MiB of weights.  Ignored otherwise. */
-    LEAN_FLAG_X_PLANES = 2u
+    LEAN_FLAG_X_PLANES = 2u,
+    /* M = 1: use the streaming kernel (a TMA-fed ring per SM; with a
+     * workspace, K split evenly over all SMs) even for products that fit the
+     * GPU in one wave, which otherwise run on a kernel that loads all of its
+     * weights before it waits for x and reduces on chip (the lower latency
+     * for one product of up to a few tens of MB).  Large products and calls
+     * that take x as planes always stream. */
+    LEAN_FLAG_STREAM = 4u
 };
 
 /* lean_qmatmul with launch flags (LEAN_FLAG_*; unknown bits are rejected

@@ -140,12 +140,13 @@ def test_streams_and_graph_capture(lean):
     check_close(yd.cpu().numpy().astype(np.float64), y_ref, bound, "graph replay")
 
 
-@pytest.mark.parametrize("M", [1, 3])
-def test_early_weights_chain_orders_x(lean, M):
+@pytest.mark.parametrize("M,extra", [(1, 0), (1, 4), (3, 0)], ids=["m1_one_wave", "m1_stream", "m3"])
+def test_early_weights_chain_orders_x(lean, M, extra):
     """A chain y_{i+1} = W_i y_i with programmatic dependent launch: each
     product must read its x only after the previous one wrote it.  The chain is
     run with and without the flag (and inside a CUDA graph); results must match
-    bit for bit, and the buffers start as NaN so a premature read shows."""
+    bit for bit, and the buffers start as NaN so a premature read shows.  M = 1
+    on the one-wave kernel and (LEAN_FLAG_STREAM) on the streaming kernel."""
     torch = torch_cuda()
     fmt, N = syn.Q4_0, 960
     steps = 24
@@ -167,8 +168,8 @@ def test_early_weights_chain_orders_x(lean, M):
 
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        ref = chain(0, s)
-        pdl = chain(lean.LEAN_FLAG_EARLY_WEIGHTS, s)
+        ref = chain(extra, s)
+        pdl = chain(lean.LEAN_FLAG_EARLY_WEIGHTS | extra, s)
     s.synchronize()
     for a, b in zip(ref, pdl):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
@@ -182,7 +183,7 @@ def test_early_weights_chain_orders_x(lean, M):
             cur = x0d
             for i in range(steps):
                 lean.lean_qmatmul_ex(fmt, Ws[i], cur, bufs[i], N, N, M,
-                                     lean.LEAN_FLAG_EARLY_WEIGHTS, s)
+                                     lean.LEAN_FLAG_EARLY_WEIGHTS | extra, s)
                 cur = bufs[i]
     for _ in range(3):
         for b in bufs:
@@ -201,8 +202,11 @@ def test_flags_rejected(lean):
     xd = torch.from_numpy(x).cuda()
     yd = torch.empty((1, N), device="cuda")
     st = torch.cuda.current_stream().cuda_stream
-    assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, 4,
+    assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, 8,
                                      st) == lean.LEAN_ERR_FORMAT
+    # the streaming-kernel flag is known
+    assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1,
+                                     lean.LEAN_FLAG_STREAM, st) == lean.LEAN_OK
     # the x-planes flag is known (and ignored without a workspace)
     assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1,
                                      lean.LEAN_FLAG_X_PLANES, st) == lean.LEAN_OK
@@ -216,11 +220,13 @@ WS_SHAPES = [(1, 1), (33, 3), (64, 43), (100, 17), (32, 200), (65, 9)]
 
 @pytest.mark.parametrize("fmt", FMTS, ids=IDS)
 @pytest.mark.parametrize("N,nblk", WS_SHAPES)
-@pytest.mark.parametrize("flags", [0, 2], ids=["fp32_x", "x_planes"])
+@pytest.mark.parametrize("flags", [0, 2, 4], ids=["one_wave", "x_planes", "stream_fp32_x"])
 def test_workspace_split_groups(lean, fmt, N, nblk, flags):
-    """M = 1 with a workspace: row groups split between CTAs are completed by
-    the last CTA; two calls in a row (the counters must come back zeroed);
-    x as fp32 or as integer planes (dp4a; Q6_K ignores the flag)."""
+    """M = 1 with a workspace: on the streaming kernel (LEAN_FLAG_STREAM, or x
+    as integer planes: dp4a, Q6_K ignores that flag) row groups split between
+    CTAs are completed by the last CTA; two calls in a row (the counters must
+    come back zeroed); without either flag these shapes take the one-wave
+    kernel, which leaves the workspace alone."""
     torch = torch_cuda()
     be = syn.BLOCK_ELEMS[fmt]
     if fmt == syn.Q6_K:
@@ -250,7 +256,9 @@ def test_workspace_split_groups(lean, fmt, N, nblk, flags):
 
 
 @pytest.mark.parametrize("fmt", FMTS, ids=IDS)
-@pytest.mark.parametrize("use_ws", [0, 1, 2], ids=["whole_groups", "workspace", "x_planes"])
+@pytest.mark.parametrize("use_ws", [0, 1, 2, 3, 4],
+                         ids=["one_wave", "one_wave_ws", "x_planes", "stream_whole_groups",
+                              "stream_workspace"])
 def test_batch(lean, fmt, use_ws):
     torch = torch_cuda()
     be = syn.BLOCK_ELEMS[fmt]
@@ -269,13 +277,14 @@ def test_batch(lean, fmt, use_ws):
         refs.append(oracle.qmatmul(fmt, W, x, N, K))
     probs = lean.make_problems(items)
     ws, nb = None, 0
-    if use_ws:
+    if use_ws in (1, 2, 4):
         nb = lean.lean_batch_workspace_bytes(fmt, probs)
         ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
     for rep in range(2):
         for it in items:
             it[2].fill_(float("nan"))
-        flags = lean.LEAN_FLAG_EARLY_WEIGHTS | (lean.LEAN_FLAG_X_PLANES if use_ws == 2 else 0)
+        flags = lean.LEAN_FLAG_EARLY_WEIGHTS | (lean.LEAN_FLAG_X_PLANES if use_ws == 2 else 0) | \
+            (lean.LEAN_FLAG_STREAM if use_ws >= 3 else 0)
         lean.lean_qmatmul_batch(fmt, probs, flags, ws, nb)
         torch.cuda.synchronize()
         for (Wd, xd, yd, N, K), (y_ref, bound) in zip(items, refs):
