@@ -78,6 +78,10 @@ def _configure(lib):
     lib.oracle_quantize.restype = c_int
     lib.oracle_double_to_fp16.argtypes = [ctypes.c_double]
     lib.oracle_double_to_fp16.restype = c_int
+    lib.oracle_quantize_x_int8.argtypes = [vp, vp, vp, c_i64, c_i64]
+    lib.oracle_quantize_x_int8.restype = c_int
+    lib.oracle_qmatmul_x_int8.argtypes = [c_int, vp, vp, vp, vp, c_i64, c_i64, c_i64]
+    lib.oracle_qmatmul_x_int8.restype = c_int
     return lib
 
 
@@ -196,3 +200,30 @@ def quantize(fmt: int, w: np.ndarray, N: int, K: int) -> np.ndarray:
     if _load().oracle_quantize(fmt, _ptr(w), _ptr(out), N, K):
         raise ValueError("oracle_quantize rejected the input")
     return out
+
+
+def quantize_x_int8(x: np.ndarray):
+    """x[M][K] fp32 -> (codes int8[M][K], scales fp32[M][K/32]) by the
+    activation-quantization reading in lean_oracle.c."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    x2 = x.reshape(-1, x.shape[-1])
+    M, K = x2.shape
+    xq = np.empty((M, K), np.int8)
+    sc = np.empty((M, K // 32), np.float32)
+    if _load().oracle_quantize_x_int8(_ptr(x2), _ptr(xq), _ptr(sc), M, K):
+        raise ValueError("K must be a positive multiple of 32")
+    return xq, sc
+
+
+def qmatmul_x_int8(fmt: int, W: np.ndarray, x: np.ndarray, N: int, K: int):
+    """(y[M][N], bound[M][N]) in fp64 of the product with x quantized to int8
+    per 32 elements (the reading in lean_oracle.c)."""
+    W = _check_w(fmt, W, N, K)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, K)
+    M = x.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    b = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_qmatmul_x_int8(fmt, _ptr(W), _ptr(x), _ptr(y), _ptr(b), N, K, M)
+    if rc:
+        raise ValueError("oracle_qmatmul_x_int8 failed (%d)" % rc)
+    return y, b

@@ -380,3 +380,79 @@ int oracle_double_to_fp16(double v)
     uint16_t h;
     return double_to_fp16_bits(v, &h) ? -1 : (int)h;
 }
+
+/* ---- the product with x quantized to int8 (activation quantization) ----------
+ *
+ * The "oxinfer" crate page (How it works) quantizes each matmul's activations
+ * so that its decode kernels can run int8 dot products.  It states no rule;
+ * the reading taken here is the one its Q8 weights use, with an fp32 scale:
+ * per block of 32 consecutive elements of x (along K),
+ *     s = max|x| / 127                       (fp32 division)
+ *     q = the integer nearest to x / s, ties away from zero, in -127..127
+ *                                            (x / s an fp32 division)
+ * with s = 0 and q = 0 for a block of zeros.  The product then uses the
+ * dequantized activation x~ = s * q:
+ *     y[m,n] = sum_k w[n,k] * s_b(k) * q[m,k]      (fp64)
+ *     B[m,n] = sum_k |w[n,k] * s_b(k) * q[m,k]|
+ * Both rounding decisions are fp32 operations, so any implementation that
+ * follows the rule in fp32 picks the same codes. */
+
+/* xq[32], scale of one block of 32 fp32 values (finite). */
+static void quantize_x_block(const float *x, int8_t *xq, float *scale)
+{
+    float amax = 0.0f;
+    for (int j = 0; j < 32; ++j) {
+        float a = fabsf(x[j]);
+        if (a > amax) amax = a;
+    }
+    volatile float s = amax / 127.0f;   /* an fp32 division, kept in fp32 */
+    *scale = s;
+    for (int j = 0; j < 32; ++j) {
+        if (s == 0.0f) { xq[j] = 0; continue; }
+        volatile float t = x[j] / s;      /* an fp32 division */
+        float r = roundf(t);              /* ties away from zero */
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        xq[j] = (int8_t)r;
+    }
+}
+
+/* x[M][K] fp32 -> codes xq[M][K] and scales[M][K/32].  K % 32 == 0. */
+int oracle_quantize_x_int8(const float *x, int8_t *xq, float *scales, int64_t M, int64_t K)
+{
+    if (K <= 0 || K % 32 != 0 || M < 0) return -1;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t b = 0; b < K / 32; ++b)
+            quantize_x_block(x + m * K + 32 * b, xq + m * K + 32 * b, scales + m * (K / 32) + b);
+    return 0;
+}
+
+/* y, bound of the product with x quantized as above. */
+int oracle_qmatmul_x_int8(int fmt, const uint8_t *W, const float *x, double *y, double *bound,
+                          int64_t N, int64_t K, int64_t M)
+{
+    int be = oracle_block_elems(fmt), bb = oracle_block_bytes(fmt);
+    if (be == 0 || K <= 0 || K % be != 0 || K % 32 != 0 || M < 0) return -1;
+    int8_t *xq = (int8_t *)malloc((size_t)(M * K));
+    float *sc = (float *)malloc(sizeof(float) * (size_t)(M * (K / 32) + 1));
+    double *w = (double *)malloc(sizeof(double) * (size_t)K);
+    if (!xq || !sc || !w) { free(xq); free(sc); free(w); return -2; }
+    oracle_quantize_x_int8(x, xq, sc, M, K);
+    int64_t row_bytes = (K / be) * bb;
+    for (int64_t n = 0; n < N; ++n) {
+        oracle_dequant_row(fmt, W + n * row_bytes, K, w);
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double xt = (double)sc[m * (K / 32) + k / 32] * (double)xq[m * K + k];
+                double p = w[k] * xt;
+                acc += p;
+                mag += fabs(p);
+            }
+            y[m * N + n] = acc;
+            if (bound) bound[m * N + n] = mag;
+        }
+    }
+    free(xq); free(sc); free(w);
+    return 0;
+}

@@ -14,6 +14,7 @@ import pytest
 import oracle
 import test_oracle_pins as P
 import test_oracle_quant_pins as QP
+import test_oracle_x_int8_pins as XP
 
 Q4_0, Q8_0, I8_B64, Q6_K = oracle.Q4_0, oracle.Q8_0, oracle.I8_B64, oracle.Q6_K
 
@@ -56,14 +57,14 @@ MUTANTS = [
      "return sign ? -v : v;",
      "return v;"),
     ("accumulation drops the running sum",
-     "                acc += p;\n",
-     "                acc = p;\n"),
+     "double p = w[k] * (double)xm[k];\n                acc += p;\n",
+     "double p = w[k] * (double)xm[k];\n                acc = p;\n"),
     ("accumulation in fp32",
-     "                acc += p;\n",
-     "                acc = (double)((float)acc + (float)p);\n"),
+     "double p = w[k] * (double)xm[k];\n                acc += p;\n",
+     "double p = w[k] * (double)xm[k];\n                acc = (double)((float)acc + (float)p);\n"),
     ("bound without the absolute value",
-     "                mag += fabs(p);\n",
-     "                mag += p;\n"),
+     "acc += p;\n                mag += fabs(p);\n            }\n            j->y",
+     "acc += p;\n                mag += p;\n            }\n            j->y"),
     ("x read transposed",
      "const float *xm = j->x + m * j->K;",
      "const float *xm = j->x + m;"),
@@ -92,6 +93,19 @@ MUTANTS = [
     ("quantizer: clamps at -128",
      "if (q < -127.0) q = -127.0;",
      "if (q < -128.0) q = -128.0;"),
+    # the activation quantization (x to int8)
+    ("x int8: ties to even",
+     "float r = roundf(t);              /* ties away from zero */",
+     "float r = rintf(t);"),
+    ("x int8: scale /128",
+     "volatile float s = amax / 127.0f;",
+     "volatile float s = amax / 128.0f;"),
+    ("x int8: scale of the wrong block",
+     "double xt = (double)sc[m * (K / 32) + k / 32] * (double)xq[m * K + k];",
+     "double xt = (double)sc[m * (K / 32) + k / 64] * (double)xq[m * K + k];"),
+    ("x int8: unquantized x in the product",
+     "double xt = (double)sc[m * (K / 32) + k / 32] * (double)xq[m * K + k];",
+     "double xt = (double)x[m * K + k];"),
 ]
 
 # The pins, with the arguments of one case each (the cheap ones).
@@ -121,6 +135,11 @@ PINS = [
     (QP.test_each_code_is_the_nearest, {"fmt": Q4_0, "be": 32}),
     (QP.test_each_code_is_the_nearest, {"fmt": Q8_0, "be": 32}),
     (QP.test_round_trip_error_bound, {"fmt": I8_B64, "be": 64}),
+    (XP.test_exact_multiples_reduce_to_the_fp32_product, {"fmt": Q8_0}),
+    (XP.test_codes_within_half_a_step, {}),
+    (XP.test_ties_go_away_from_zero, {}),
+    (XP.test_zero_block_and_scaling_and_sign, {}),
+    (XP.test_within_the_quantization_bound_of_the_exact_product, {"fmt": Q4_0}),
 ]
 
 
