@@ -551,13 +551,15 @@ def main():
                    "timing": "CUDA events on the launching stream; a ~1 ms GPU sleep precedes "
                              "the first event so the host has enqueued the timed steps",
                    "parallelism": "replicas" if ws > 1 else "single GPU"})
-    per_config = dependent = None
+    per_config = dependent = x_int8 = None
     if ws == 1 and not args.no_per_config and args.workload == "decode_stack":
         import torch
         device = torch.device("cuda", local)
         stream = torch.cuda.Stream(device)
         dependent = time_dependent_step(device, r["l2"], stream, min(args.steps, 200),
                                         max(3, min(args.warmup, 20)))
+        x_int8 = time_step_x_int8(device, r["l2"], stream, min(args.steps, 1000),
+                                  max(3, min(args.warmup, 20)))
         per_config = time_per_config(device, r["l2"], stream)
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
@@ -589,6 +591,8 @@ def main():
         "spot_check_vs_oracle": r["spot_ok"],
         # the same decode step with each layer's dependencies kept (128 calls)
         "decode_step_layer_order": dependent,
+        # the same step with x quantized to int8 (an approximate product)
+        "decode_step_x_int8": x_int8,
         # every other workload, one product at a time (CUDA events, weights
         # rotating beyond L2); frac against the measured HBM peak
         "per_config": per_config,
@@ -746,6 +750,53 @@ def time_dependent_step(device, l2, stream, steps, warmup):
             "calls_per_step": calls_per_step, "launches_per_step": calls_per_step,
             "ms_per_step": ms, "GB/s": gbs, "frac": gbs / peak,
             "linears_per_s": len(lins) / (ms * 1e-3), "steps": steps, "warmup": warmup}
+
+
+def time_step_x_int8(device, l2, stream, steps, warmup):
+    """The SmolLM2-360M decode step as one batch call with x quantized to int8
+    per 32 elements (LEAN_FLAG_X_INT8, the "oxinfer" page's activation
+    quantization): a different, approximate product, timed beside the exact
+    one."""
+    import torch
+    from block_quantized_weight_dot_gb300 import lean
+    wl = syn.smollm2_360m_decode_stack()
+    dw = DeviceWorkload(wl, device, l2)
+    flags = lean.LEAN_FLAG_EARLY_WEIGHTS | lean.LEAN_FLAG_X_INT8
+
+    def step(c):
+        lean.lean_qmatmul_batch(dw.lins[0].fmt, dw.batch[c], flags, dw.ws, dw.ws_bytes, stream)
+
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    graphs = []
+    for c in range(dw.copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                step(c)
+        graphs.append(g)
+    for s in range(warmup):
+        graphs[s % dw.copies].replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HEAD_START_CYCLES)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for s in range(steps):
+            graphs[s % dw.copies].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    peak, _ = measured_peaks()
+    gbs = wl.algorithmic_bytes / (ms * 1e-3) / 1e9
+    del dw, graphs
+    torch.cuda.empty_cache()
+    return {"workload": wl.name + "_x_int8", "ms_per_step": ms, "GB/s": gbs, "frac": gbs / peak,
+            "launches_per_step": 2, "steps": steps, "warmup": warmup,
+            "numerics": "x quantized to int8 per 32 elements (s = max|x|/127); not the exact "
+                        "product"}
 
 
 def sweep(args):

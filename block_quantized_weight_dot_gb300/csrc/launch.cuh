@@ -505,7 +505,8 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
                 max_nb = std::max<int>(max_nb, (int)(ph[i].g.K / 32));
             }
         }
-        use_planes = xqb > 0 && (wbytes >= kPlanesMinWeightBytes || (flags & LEAN_FLAG_X_PLANES));
+        use_planes = xqb > 0 && (wbytes >= kPlanesMinWeightBytes ||
+                                 (flags & (LEAN_FLAG_X_PLANES | LEAN_FLAG_X_INT8)));
         const WorkspaceLayout wl = workspace_layout(groups, xqb, n > 1);
         if (ws_bytes < wl.total) return LEAN_ERR_SHAPE;
         const int cps = use_planes ? StreamRing<FMT, true>::CPS : StreamRing<FMT, false>::CPS;
@@ -524,7 +525,7 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
         if (use_planes) {
             XprepArgs<NP> xa;
             xa.nprob = n;
-            xa.pad = 0;
+            xa.int8 = (flags & LEAN_FLAG_X_INT8) ? 1 : 0;
             xa.xq = static_cast<uint8_t *>(ws) + wl.xq_off;
             for (int i = 0; i < n; ++i) {
                 xa.p[i].x = ph[i].x;
@@ -538,7 +539,7 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
             cfg.blockDim = dim3(256, 1, 1);
             cfg.stream = stream;
             cudaLaunchAttribute attr[2];
-            fill_launch(cfg, attr, 1, flags);
+            fill_launch(cfg, attr, 1, flags & LEAN_FLAG_EARLY_WEIGHTS);
             if (cudaLaunchKernelEx(&cfg, xprep_kernel<FMT, NP>, xa) != cudaSuccess)
                 return LEAN_ERR_CUDA;
             a.xq = xa.xq;

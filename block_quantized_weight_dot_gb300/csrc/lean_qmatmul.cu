@@ -85,8 +85,13 @@ lean_status dispatch_m1(int fmt, const HostProb *ph, int n, unsigned flags, void
     // a workspace smaller than the size query gives is refused whichever
     // kernel runs
     if (ws && wsb < workspace_layout(groups, xqb, n > 1).total) return LEAN_ERR_SHAPE;
+    if (flags & LEAN_FLAG_X_INT8) {  // x quantized to int8: needs the planes' workspace
+        if (fmt == LEAN_Q6_K) return LEAN_ERR_FORMAT;
+        if (!ws) return LEAN_ERR_NULL;
+    }
     const bool planes = ws && fmt != LEAN_Q6_K &&
-                        ((flags & LEAN_FLAG_X_PLANES) || wbytes >= kPlanesMinWeightBytes);
+                        ((flags & (LEAN_FLAG_X_PLANES | LEAN_FLAG_X_INT8)) ||
+                         wbytes >= kPlanesMinWeightBytes);
     if (!(flags & LEAN_FLAG_STREAM) && !planes) {
         bool done = false;
         lean_status st = LEAN_OK;
@@ -108,8 +113,10 @@ lean_status check_product(int fmt, const void *W, const float *x, const float *y
     if (M > ((int64_t)1 << 31) / std::max<int64_t>(K, N)) return LEAN_ERR_SHAPE;
     if (!W || !x || !y) return LEAN_ERR_NULL;
     if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return LEAN_ERR_ALIGN;
-    if (flags & ~(unsigned)(LEAN_FLAG_EARLY_WEIGHTS | LEAN_FLAG_X_PLANES | LEAN_FLAG_STREAM))
+    if (flags & ~(unsigned)(LEAN_FLAG_EARLY_WEIGHTS | LEAN_FLAG_X_PLANES | LEAN_FLAG_STREAM |
+                            LEAN_FLAG_X_INT8))
         return LEAN_ERR_FORMAT;
+    if ((flags & LEAN_FLAG_X_INT8) && M != 1) return LEAN_ERR_FORMAT;
     return LEAN_OK;
 }
 

@@ -55,6 +55,7 @@ lean_status lean_qmatmul_fixed_ws(int fmt, const void *W_packed_dev, const float
                                   float *y_dev, int64_t N, int64_t K, unsigned flags,
                                   void *stream) {
     if (block_elems(fmt) == 0) return LEAN_ERR_FORMAT;
+    if (flags & LEAN_FLAG_X_INT8) return LEAN_ERR_FORMAT;  // no room for x codes in the array
     Geom g;
     if (!make_geom(fmt, N, K, &g)) return LEAN_ERR_SHAPE;
     const WorkspaceLayout wl = workspace_layout(g.groups);

@@ -324,6 +324,29 @@ __device__ __forceinline__ XBlock x_block_quantize(float v) {
           : r.tier == 1 ? __float2int_rn(rf) : 0;
     return r;
 }
+// x quantized to int8 (LEAN_FLAG_X_INT8), one block: s = max|v| / 127 and
+// q = round(v / s), ties away from zero, both fp32 operations as the rule
+// states (0 for a block of zeros); the codes go in the top plane (chunk tier
+// 3: the consumers read that plane only) with scale s (1/16 more for Q4_0).
+// A block holding an Inf or NaN gets a NaN scale.
+template <int FMT>
+__device__ __forceinline__ void x_block_store_int8(float v, uint8_t *dst, int lane) {
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
+    const float amax = __uint_as_float(mx);
+    const float s = __fdiv_rn(amax, 127.f);
+    int q = 0;
+    if (mx != 0u && mx < 0x7f800000u)
+        q = (int)fminf(fmaxf(roundf(__fdiv_rn(v, s)), -127.f), 127.f);
+    dst[kXqHeader + plane_pos<FMT>(lane)] = (uint8_t)q;
+    const int sq = __reduce_add_sync(0xffffffffu, q);
+    if (lane == 0) {
+        const float scale = mx >= 0x7f800000u ? __int_as_float(0x7fc00000)
+                                              : (FMT == Q4_0 ? s * (1.f / 16.f) : s);
+        reinterpret_cast<int4 *>(dst)[0] = make_int4(-128 * sq, 0, 0, 0);
+        reinterpret_cast<int4 *>(dst)[1] = make_int4(__float_as_int(scale), 3, 0, 0);
+    }
+}
+
 // Writes the block's planes at dst: the bytes of X, X = X3*2^24 + X2*2^16 +
 // X1*2^8 + X0 with X3 signed and the others in 0..255, each plane's header
 // init -128 * (its byte sum), the block's scale and the chunk's tier `mode`.
@@ -365,7 +388,7 @@ struct XprepProb {
 template <int NP>
 struct XprepArgs {
     int nprob;
-    int pad;
+    int int8;  // 1: quantize x to int8 (LEAN_FLAG_X_INT8) instead of the exact planes
     uint8_t *xq;
     XprepProb p[NP];
 };
@@ -384,6 +407,13 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ Xpre
 #pragma unroll
     for (int u = 0; u < kXprepBlocks; ++u)
         v[u] = b0 + u < p.nb ? p.x[32 * (int64_t)(b0 + u) + lane] : 0.f;
+    if (a.int8) {
+#pragma unroll
+        for (int u = 0; u < kXprepBlocks; ++u)
+            if (b0 + u < p.nb)
+                x_block_store_int8<FMT>(v[u], a.xq + p.xq0 + (int64_t)(b0 + u) * kXqBytes, lane);
+        return;
+    }
     XBlock xb[kXprepBlocks];
 #pragma unroll
     for (int u = 0; u < kXprepBlocks; ++u) {
@@ -416,16 +446,28 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
 // plane order: w[0..7] hold four raw weight bytes each.  The even words start
 // their chains at 0 and the odd ones at the header's -128 * (plane byte sum);
 // LO16 scales the even chains by 16 (Q4_0: the even words hold the low
-// nibbles, the odd ones the high nibbles in place, i.e. 16 * q).  FINE: the
-// lowest plane may be nonzero (tier 1), else it is all zero and skipped.
-// Returns the block's exact sum of (weight byte - offset) * X (times 16 for
-// Q4_0), rounded once to fp32.
-template <bool LO16, bool FINE>
+// nibbles, the odd ones the high nibbles in place, i.e. 16 * q).  TIER 1: the
+// lowest plane may be nonzero, else (0) it is all zero and skipped; TIER 3:
+// x as int8 codes, in the top plane alone.  Returns the block's exact sum of
+// (weight byte - offset) * X (times 16 for Q4_0), rounded once to fp32.
+template <bool LO16, int TIER>
 __device__ __forceinline__ float plane_dot(const uint32_t (&w)[8], const uint8_t *xq) {
+    constexpr bool FINE = TIER == 1;
+    constexpr int L = LO16 ? 16 : 1;
     const int4 h = *reinterpret_cast<const int4 *>(xq);
     const uint4 *pl = reinterpret_cast<const uint4 *>(xq + kXqHeader);
-    const uint4 a3 = pl[0], b3 = pl[1], a2 = pl[2], b2 = pl[3], a1 = pl[4], b1 = pl[5];
+    const uint4 a3 = pl[0], b3 = pl[1];
     const uint32_t P3[8] = {a3.x, a3.y, a3.z, a3.w, b3.x, b3.y, b3.z, b3.w};
+    if (TIER == 3) {  // x as int8 codes: the top plane alone
+        uint32_t s3 = 0, t3 = (uint32_t)h.x;
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            s3 = dp4a_us(w[i], P3[i], s3);
+            t3 = dp4a_us(w[i + 1], P3[i + 1], t3);
+        }
+        return (float)((int)s3 * L + (int)t3);  // |.| < 2^20: exact
+    }
+    const uint4 a2 = pl[2], b2 = pl[3], a1 = pl[4], b1 = pl[5];
     const uint32_t P2[8] = {a2.x, a2.y, a2.z, a2.w, b2.x, b2.y, b2.z, b2.w};
     const uint32_t P1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
     uint32_t P0[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -449,7 +491,6 @@ __device__ __forceinline__ float plane_dot(const uint32_t (&w)[8], const uint8_t
             t0 = dp4a_uu(w[i + 1], P0[i + 1], t0);
         }
     }
-    constexpr int L = LO16 ? 16 : 1;
     const int u3 = (int)s3 * L + (int)t3, u2 = (int)s2 * L + (int)t2, u1 = (int)s1 * L + (int)t1;
     const int u0 = FINE ? (int)s0 * L + (int)t0 : 0;
     // |u| < 2^21, so both halves are exact in int32.  T = hi * 2^16 + lo is
@@ -492,7 +533,7 @@ __device__ __noinline__ float exact_block_dot(uint4 wa, uint4 wb, float d, const
 // d * 2^-sf (the two scales first, so that only a result beyond the fp32
 // range can overflow).  MODE is the chunk's tier: 0 all blocks on the coarse
 // grid, 1 some on the fine grid, 2 some marked for the exact fp32 dot (this
-// block's own scale, -1 when marked, decides).
+// block's own scale, -1 when marked, decides), 3 x quantized to int8 codes.
 template <int FMT, int MODE>
 __device__ __forceinline__ float x_block_dot(const uint32_t (&w)[8], float d, const uint8_t *xq,
                                              const float *xg) {
@@ -500,7 +541,7 @@ __device__ __forceinline__ float x_block_dot(const uint32_t (&w)[8], float d, co
     if (MODE == 2 && scale < 0.f)
         return exact_block_dot<FMT>(make_uint4(w[0], w[1], w[2], w[3]),
                                     make_uint4(w[4], w[5], w[6], w[7]), d, xg);
-    return (d * scale) * plane_dot<FMT == Q4_0, MODE != 0>(w, xq);
+    return (d * scale) * plane_dot<FMT == Q4_0, MODE == 2 ? 1 : MODE>(w, xq);
 }
 // One block with x as planes: this lane's row, block b of the step at ws, x
 // planes of the chunk at xq, fp32 x of the chunk at xg.
@@ -543,7 +584,7 @@ __device__ __forceinline__ float planes_chunk(const uint8_t *ws, const uint8_t *
 #pragma unroll
         for (int i = 0; i < C::BPC; ++i)
             acc += block_dot_q<FMT, MODE>(ws, xq, xg, i, scale_of(sv, sub * C::BPC + i), lane);
-    } else if (MODE == 0) {
+    } else if (MODE == 0 || MODE == 3) {
 #pragma unroll
         for (int i = 0; i < C::BPC; ++i)
             if (i < nbc)
@@ -649,6 +690,7 @@ __device__ __forceinline__ float consume_chunk(const uint8_t *ws, const float *x
         const int mode = *reinterpret_cast<const int *>(xq + 20);  // the chunk's tier
         if (mode == 0) return planes_chunk<FMT, 0>(ws, xq, xg, sv, nbc, sub, lane);
         if (mode == 1) return planes_chunk<FMT, 1>(ws, xq, xg, sv, nbc, sub, lane);
+        if (mode == 3) return planes_chunk<FMT, 3>(ws, xq, xg, sv, nbc, sub, lane);
         return planes_chunk<FMT, 2>(ws, xq, xg, sv, nbc, sub, lane);
     }
     if (nbc == C::BPC) {

@@ -22,6 +22,7 @@ LEAN_OK, LEAN_ERR_FORMAT, LEAN_ERR_SHAPE, LEAN_ERR_NULL, LEAN_ERR_ALIGN, LEAN_ER
 LEAN_FLAG_EARLY_WEIGHTS = 1
 LEAN_FLAG_X_PLANES = 2
 LEAN_FLAG_STREAM = 4
+LEAN_FLAG_X_INT8 = 8
 
 # every symbol the header declares, with (restype, argtypes)
 _i64, _int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p

@@ -180,7 +180,17 @@ enum {
      * weights before it waits for x and reduces on chip (the lower latency
      * for one product of up to a few tens of MB).  Large products and calls
      * that take x as planes always stream. */
-    LEAN_FLAG_STREAM = 4u
+    LEAN_FLAG_STREAM = 4u,
+    /* M = 1 with a workspace, Q4_0 / Q8_0 / I8_B64 (LEAN_ERR_FORMAT for Q6_K
+     * or M != 1, LEAN_ERR_NULL without a workspace): quantize x to int8 per
+     * 32 elements and take int8 dot products, as the "oxinfer" crate page's
+     * decode kernels do (How it works: per-matmul activation quantization,
+     * int8 SDOT).  Rule: s = max|x| / 127 and q = round(x / s), ties away from
+     * zero, both fp32 operations, q in -127..127 (s = 0, q = 0 for a block of
+     * zeros).  y is then the product of w with x~ = s * q, not with x: about
+     * 1e-3 .. 1e-2 of |y| away from the fp32-x result, and within 1e-4 *
+     * sum_k |w x~| + 1e-6 of the exact product with x~.  x must be finite. */
+    LEAN_FLAG_X_INT8 = 8u
 };
 
 /* lean_qmatmul with launch flags (LEAN_FLAG_*; unknown bits are rejected
@@ -277,7 +287,8 @@ lean_status lean_qmatmul_batch(int fmt, int count, const lean_problem *problems,
  * must use a host framework's pool, loops that may not risk the
  * synchronisation of cudaMalloc / cudaFree).
  *   - Accepts N up to 8388608 rows (262144 row groups); larger N returns
- *     LEAN_ERR_SHAPE.  W, x, y, flags and stream as for lean_qmatmul_ex.
+ *     LEAN_ERR_SHAPE.  W, x, y, flags and stream as for lean_qmatmul_ex, x in
+ *     fp32 always (LEAN_FLAG_X_INT8 returns LEAN_ERR_FORMAT).
  *   - The first call on a device looks up the array's device address (and
  *     may load the library's kernels); make it before any stream capture.
  *   - Every call uses the same array: it clears the arrival counters it needs

@@ -26,6 +26,8 @@ def test_default_line_has_the_contract_fields(monkeypatch):
     monkeypatch.setattr(bench, "time_per_config", lambda device, l2, stream: list(per))
     monkeypatch.setattr(bench, "time_dependent_step",
                         lambda device, l2, stream, steps, warmup: dict(dep))
+    monkeypatch.setattr(bench, "time_step_x_int8",
+                        lambda device, l2, stream, steps, warmup: {"ms_per_step": 0.03})
     import torch
     monkeypatch.setattr(torch.cuda, "Stream", lambda device=None: None)
     monkeypatch.setattr(sys, "argv", ["bench.py", "--no-cpu-baseline", "--steps", "5",
@@ -55,3 +57,4 @@ def test_default_line_has_the_contract_fields(monkeypatch):
     assert [p["config"] for p in line["per_config"]] == [p["config"] for p in per]
     assert line["per_config"][1]["tensor_pipe"]["frac_of_bf16_peak"] == 0.2
     assert line["decode_step_layer_order"]["calls_per_step"] == 128
+    assert line["decode_step_x_int8"]["ms_per_step"] == 0.03

@@ -202,7 +202,7 @@ def test_flags_rejected(lean):
     xd = torch.from_numpy(x).cuda()
     yd = torch.empty((1, N), device="cuda")
     st = torch.cuda.current_stream().cuda_stream
-    assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, 8,
+    assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1, 16,
                                      st) == lean.LEAN_ERR_FORMAT
     # the streaming-kernel flag is known
     assert lean._lib.lean_qmatmul_ex(0, Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), N, K, 1,
