@@ -82,6 +82,10 @@ def _configure(lib):
     lib.oracle_quantize_x_int8.restype = c_int
     lib.oracle_qmatmul_x_int8.argtypes = [c_int, vp, vp, vp, vp, c_i64, c_i64, c_i64]
     lib.oracle_qmatmul_x_int8.restype = c_int
+    lib.oracle_silu.argtypes = [ctypes.c_double]
+    lib.oracle_silu.restype = ctypes.c_double
+    lib.oracle_swiglu.argtypes = [c_int, vp, vp, vp, vp, vp, vp, vp, vp, c_i64, c_i64]
+    lib.oracle_swiglu.restype = c_int
     return lib
 
 
@@ -227,3 +231,23 @@ def qmatmul_x_int8(fmt: int, W: np.ndarray, x: np.ndarray, N: int, K: int):
     if rc:
         raise ValueError("oracle_qmatmul_x_int8 failed (%d)" % rc)
     return y, b
+
+
+def silu(t: float) -> float:
+    """t / (1 + e^-t) in fp64."""
+    return _load().oracle_silu(float(t))
+
+
+def swiglu(fmt: int, Wg: np.ndarray, Wu: np.ndarray, x: np.ndarray, N: int, K: int):
+    """h = silu(W_gate x) * (W_up x) for one x[K]; returns (h, g, u, bound_g,
+    bound_u), each fp64 [N]."""
+    Wg = _check_w(fmt, Wg, N, K)
+    Wu = _check_w(fmt, Wu, N, K)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    if x.size != K:
+        raise ValueError("x must have K elements")
+    out = [np.empty(N, dtype=np.float64) for _ in range(5)]
+    rc = _load().oracle_swiglu(fmt, _ptr(Wg), _ptr(Wu), _ptr(x), *[_ptr(a) for a in out], N, K)
+    if rc:
+        raise ValueError("oracle_swiglu failed (%d)" % rc)
+    return tuple(out)

@@ -456,3 +456,27 @@ int oracle_qmatmul_x_int8(int fmt, const uint8_t *W, const float *x, double *y, 
     free(xq); free(sc); free(w);
     return 0;
 }
+
+/* ---- the gated FFN input: h = silu(W_gate x) * (W_up x) ------------------------
+ *
+ * A decode layer is N x (attention + FFN) ("wgpu-llm" README, Architecture at
+ * a Glance); the FFN of the models the pages run (SmolLM2, Qwen2.5,
+ * TinyLlama) feeds its down projection with silu(gate) * up, silu(t) =
+ * t / (1 + e^-t).  The oracle composes its own products with SiLU written from
+ * that definition, in fp64. */
+double oracle_silu(double t)
+{
+    return t / (1.0 + exp(-t));
+}
+
+/* h[n], and the parts the tolerance needs: g, u and their bounds. */
+int oracle_swiglu(int fmt, const uint8_t *Wg, const uint8_t *Wu, const float *x, double *h,
+                  double *g, double *u, double *bg, double *bu, int64_t N, int64_t K)
+{
+    int rc = oracle_qmatmul(fmt, Wg, x, g, bg, N, K, 1, 1);
+    if (rc) return rc;
+    rc = oracle_qmatmul(fmt, Wu, x, u, bu, N, K, 1, 1);
+    if (rc) return rc;
+    for (int64_t n = 0; n < N; ++n) h[n] = oracle_silu(g[n]) * u[n];
+    return 0;
+}

@@ -14,6 +14,7 @@ import pytest
 import oracle
 import test_oracle_pins as P
 import test_oracle_quant_pins as QP
+import test_oracle_swiglu_pins as SP
 import test_oracle_x_int8_pins as XP
 
 Q4_0, Q8_0, I8_B64, Q6_K = oracle.Q4_0, oracle.Q8_0, oracle.I8_B64, oracle.Q6_K
@@ -103,6 +104,13 @@ MUTANTS = [
     ("x int8: scale of the wrong block",
      "double xt = (double)sc[m * (K / 32) + k / 32] * (double)xq[m * K + k];",
      "double xt = (double)sc[m * (K / 32) + k / 64] * (double)xq[m * K + k];"),
+    # the gated FFN input
+    ("silu: sign of the exponent",
+     "return t / (1.0 + exp(-t));",
+     "return t / (1.0 + exp(t));"),
+    ("swiglu: gate and up swapped in the epilogue",
+     "h[n] = oracle_silu(g[n]) * u[n];",
+     "h[n] = oracle_silu(u[n]) * g[n];"),
     ("x int8: unquantized x in the product",
      "double xt = (double)sc[m * (K / 32) + k / 32] * (double)xq[m * K + k];",
      "double xt = (double)x[m * K + k];"),
@@ -135,6 +143,8 @@ PINS = [
     (QP.test_each_code_is_the_nearest, {"fmt": Q4_0, "be": 32}),
     (QP.test_each_code_is_the_nearest, {"fmt": Q8_0, "be": 32}),
     (QP.test_round_trip_error_bound, {"fmt": I8_B64, "be": 64}),
+    (SP.test_silu_closed_forms, {}),
+    (SP.test_swiglu_hand_built_blocks, {}),
     (XP.test_exact_multiples_reduce_to_the_fp32_product, {"fmt": Q8_0}),
     (XP.test_codes_within_half_a_step, {}),
     (XP.test_ties_go_away_from_zero, {}),
