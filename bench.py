@@ -687,34 +687,49 @@ def time_per_config(device, l2, stream):
 
 def time_dependent_step(device, l2, stream, steps, warmup):
     """The SmolLM2-360M decode step with the dependencies of a real layer kept:
-    per layer [q, k, v] (one batch call) -> o -> [gate, up] (one batch call)
-    -> down, 128 calls per step in stream order with programmatic dependent
-    launch, one CUDA graph per weight copy (the copies larger than 2x L2)."""
+    per layer [q, k, v] (one batch call) -> o -> gate / up with the SiLU(gate)
+    * up epilogue (lean_qmatmul_swiglu) -> down, which reads that h; 128 calls
+    per step in stream order with programmatic dependent launch, one CUDA
+    graph per weight copy (the copies larger than 2x L2)."""
     import torch
     from block_quantized_weight_dot_gb300 import lean
     wl = syn.smollm2_360m_decode_stack()
     dw = DeviceWorkload(wl, device, l2)
     lins = dw.lins
-    groups = [[0, 1, 2], [3], [4, 5], [6]]
+    fmt = lins[0].fmt
     flags = lean.LEAN_FLAG_EARLY_WEIGHTS
+    layers = len(lins) // 7
+    hbuf = torch.empty((layers, lins[4].N), dtype=torch.float32, device=device)
+    xp = lambda i: dw.x.data_ptr() + 4 * dw.x_off[i]
+    yp = lambda i: dw.y.data_ptr() + 4 * dw.y_off[i]
 
-    def calls(c):
+    def plan(c):
         out = []
-        for layer in range(len(lins) // 7):
-            for grp in groups:
-                idx = [7 * layer + j for j in grp]
-                out.append(lean.make_problems(
-                    [(dw.W[c][i], dw.x.data_ptr() + 4 * dw.x_off[i],
-                      dw.y.data_ptr() + 4 * dw.y_off[i], lins[i].N, lins[i].K) for i in idx]))
+        for l in range(layers):
+            i = 7 * l
+            qkv = lean.make_problems([(dw.W[c][i + j], xp(i + j), yp(i + j), lins[i + j].N,
+                                       lins[i + j].K) for j in (0, 1, 2)])
+            o = lean.make_problems([(dw.W[c][i + 3], xp(i + 3), yp(i + 3), lins[i + 3].N,
+                                     lins[i + 3].K)])
+            # gate (i + 4) and up (i + 5) read the gate linear's x; down reads h
+            gu = (dw.W[c][i + 4], dw.W[c][i + 5], xp(i + 4), hbuf[l].data_ptr(), lins[i + 4].N,
+                  lins[i + 4].K)
+            down = lean.make_problems([(dw.W[c][i + 6], hbuf[l].data_ptr(), yp(i + 6),
+                                        lins[i + 6].N, lins[i + 6].K)])
+            out.append((qkv, o, gu, down))
         return out
 
-    plan = [calls(c) for c in range(dw.copies)]
-    wsb = max(lean.lean_batch_workspace_bytes(lins[0].fmt, p) for p in plan[0])
+    plans = [plan(c) for c in range(dw.copies)]
+    wsb = max(max(lean.lean_batch_workspace_bytes(fmt, p) for p in (qkv, o, down))
+              for qkv, o, _, down in plans[0])
     ws = torch.zeros(max(256, wsb), dtype=torch.uint8, device=device)
 
     def step(c):
-        for probs in plan[c]:
-            lean.lean_qmatmul_batch(lins[0].fmt, probs, flags, ws, wsb, stream)
+        for qkv, o, gu, down in plans[c]:
+            lean.lean_qmatmul_batch(fmt, qkv, flags, ws, wsb, stream)
+            lean.lean_qmatmul_batch(fmt, o, flags, ws, wsb, stream)
+            lean.lean_qmatmul_swiglu(fmt, *gu, flags, stream)
+            lean.lean_qmatmul_batch(fmt, down, flags, ws, wsb, stream)
 
     with torch.cuda.stream(stream):
         step(0)
@@ -740,15 +755,19 @@ def time_dependent_step(device, l2, stream, steps, warmup):
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1) / steps
     peak, _ = measured_peaks()
-    gbs = wl.algorithmic_bytes / (ms * 1e-3) / 1e9
-    calls_per_step = len(plan[0])
+    # bytes: the step's weights, each call's x once and y once (h counted as
+    # the swiglu output and the down input)
+    alg = wl.algorithmic_bytes - 4 * layers * lins[5].K
+    gbs = alg / (ms * 1e-3) / 1e9
+    calls_per_step = 4 * layers
     del dw, graphs
     torch.cuda.empty_cache()
     return {"workload": wl.name + "_layer_order",
-            "order": "per layer: [q,k,v] batch -> o -> [gate,up] batch -> down (stream order, "
-                     "programmatic dependent launch)",
+            "order": "per layer: [q,k,v] batch -> o -> gate/up with the SiLU(gate)*up epilogue "
+                     "(lean_qmatmul_swiglu) -> down reading that h (stream order, programmatic "
+                     "dependent launch)",
             "calls_per_step": calls_per_step, "launches_per_step": calls_per_step,
-            "ms_per_step": ms, "GB/s": gbs, "frac": gbs / peak,
+            "ms_per_step": ms, "algorithmic_bytes_per_step": alg, "GB/s": gbs, "frac": gbs / peak,
             "linears_per_s": len(lins) / (ms * 1e-3), "steps": steps, "warmup": warmup}
 
 

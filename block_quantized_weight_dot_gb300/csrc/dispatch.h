@@ -62,6 +62,9 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
 // M = 1 on the one-wave kernel; *done = false when the problems do not fit it
 template <int FMT>
 lean_status gemv_fmt(const HostProb *ph, int n, unsigned flags, cudaStream_t stream, bool *done);
+// h = silu(W_gate x) * (W_up x); ph[0] gate (its x and y are the call's), ph[1] up
+template <int FMT>
+lean_status swiglu_fmt(const HostProb *ph, unsigned flags, cudaStream_t stream);
 // planes: with a workspace, hand x to the integer formats as planes (dp4a)
 template <int FMT>
 lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,

@@ -306,7 +306,7 @@ inline int gemv_ctas_per_sm() {
     int v = cache[dev].load(std::memory_order_relaxed);
     if (v == 0) {
         constexpr int smem = (kGemvWarps * GemvCfg<FMT>::NB * BlockTraits<FMT>::E + 256) * 4;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, qmm_gemv_kernel<FMT, NP>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, qmm_gemv_kernel<FMT, NP, false>,
                                                           kGemvThreads, smem) != cudaSuccess ||
             v <= 0)
             v = -1;
@@ -362,8 +362,48 @@ lean_status launch_gemv(const HostProb *ph, int n, unsigned flags, cudaStream_t 
     cudaLaunchAttribute attr[2];
     fill_launch(cfg, attr, cl, flags);
     *done = true;
-    return cudaLaunchKernelEx(&cfg, qmm_gemv_kernel<FMT, NP>, a) == cudaSuccess ? LEAN_OK
-                                                                              : LEAN_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, qmm_gemv_kernel<FMT, NP, false>, a) == cudaSuccess
+               ? LEAN_OK
+               : LEAN_ERR_CUDA;
+}
+
+// h = silu(W_gate x) * (W_up x) on the one-wave kernel (any number of waves):
+// a cluster of 2 x (K split) CTAs per row group.  ph[0] gate, ph[1] up.
+template <int FMT>
+lean_status swiglu_fmt(const HostProb *ph, unsigned flags, cudaStream_t stream) {
+    constexpr int NB = GemvCfg<FMT>::NB;
+    const Geom &g = ph[0].g;
+    const int ks = (int)((g.blocks + kGemvWarps * NB - 1) / (kGemvWarps * NB));
+    if (2 * ks > kGemvMaxCluster || g.groups * 2 * ks > INT32_MAX) return LEAN_ERR_SHAPE;
+    GemvArgs<2> a;
+    a.nprob = 2;
+    a.cl = 2 * ks;
+    a.mg = make_magic();
+    for (int i = 0; i < 2; ++i) {
+        GemvProb &p = a.p[i];
+        p.W = ph[i].W;
+        p.x = ph[0].x;
+        p.y = ph[0].y;
+        p.N = (int)g.N;
+        p.K = (int)g.K;
+        p.blocks = (int)g.blocks;
+        p.steps = g.steps;
+        p.last_blocks = g.last_blocks;
+        p.step_vecs = g.step_vecs;
+        p.nbw = (int)((g.blocks + kGemvWarps * ks - 1) / (kGemvWarps * ks));
+        p.cta0 = 0;
+        p.group_vecs = g.group_vecs;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(g.groups * 2 * ks), 1, 1);
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = (kGemvWarps * NB * BlockTraits<FMT>::E + 256) * 4;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    fill_launch(cfg, attr, 2 * ks, flags);
+    return cudaLaunchKernelEx(&cfg, qmm_gemv_kernel<FMT, 2, true>, a) == cudaSuccess
+               ? LEAN_OK
+               : LEAN_ERR_CUDA;
 }
 
 template <int FMT>
@@ -580,6 +620,7 @@ lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int6
     template lean_status stream_fmt<FMT>(const HostProb *, int, unsigned, void *, int64_t,     \
                                          bool, unsigned *, cudaStream_t);                      \
     template lean_status gemv_fmt<FMT>(const HostProb *, int, unsigned, cudaStream_t, bool *); \
+    template lean_status swiglu_fmt<FMT>(const HostProb *, unsigned, cudaStream_t);              \
     template lean_status mma_fmt<FMT>(const Geom &, const uint8_t *, const float *, float *,   \
                                       int64_t, unsigned, void *, int64_t, unsigned *,          \
                                       cudaStream_t);

@@ -274,6 +274,30 @@ lean_status lean_embed_rows(int fmt, const void *W_packed_dev, const int32_t *id
     return LEAN_ERR_FORMAT;
 }
 
+lean_status lean_qmatmul_swiglu(int fmt, const void *W_gate_dev, const void *W_up_dev,
+                                const float *x_dev, float *h_dev, int64_t N, int64_t K,
+                                unsigned flags, void *stream) {
+    HostProb hp[2];
+    lean_status st = check_product(fmt, W_gate_dev, x_dev, h_dev, N, K, 1, flags, &hp[0].g);
+    if (st != LEAN_OK) return st;
+    st = check_product(fmt, W_up_dev, x_dev, h_dev, N, K, 1, flags, &hp[1].g);
+    if (st != LEAN_OK) return st;
+    if (flags & ~(unsigned)LEAN_FLAG_EARLY_WEIGHTS) return LEAN_ERR_FORMAT;
+    hp[0].W = (const uint8_t *)W_gate_dev;
+    hp[1].W = (const uint8_t *)W_up_dev;
+    hp[0].x = hp[1].x = x_dev;
+    hp[0].y = hp[1].y = h_dev;
+    cudaGetLastError();
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (fmt) {
+    case LEAN_Q4_0: return swiglu_fmt<Q4_0>(hp, flags, s);
+    case LEAN_Q8_0: return swiglu_fmt<Q8_0>(hp, flags, s);
+    case LEAN_I8_B64: return swiglu_fmt<I8_B64>(hp, flags, s);
+    case LEAN_Q6_K: return swiglu_fmt<Q6_K>(hp, flags, s);
+    }
+    return LEAN_ERR_FORMAT;
+}
+
 lean_status lean_wait_selftest(unsigned limit_us, void *stream) {
     if (limit_us < 1 || limit_us > 1000000) return LEAN_ERR_SHAPE;
     unsigned *err = error_word();

@@ -82,7 +82,12 @@ __device__ __forceinline__ void gemv_load(BlockFrag<FMT> &f, const GemvProb &p, 
 // grid.x = sum over problems of groups * cl; cluster = (cl, 1, 1);
 // blockDim.x = 256; dynamic shared memory: the CTA's x slice (8 * nbw * E
 // floats of the largest problem) then 8 x 32 partial sums.
-template <int FMT, int NP>
+// SWIGLU: the problems come in pairs (gate, up) of one shape, x and output;
+// each row group gets a cluster of cl = 2 * (K split) CTAs, the first half on
+// the gate rows, the second on the up rows, and rank 0 writes
+// h = silu(gate . x) * (up . x) (the input of the FFN's down projection).
+// A pair's two entries carry the same cta0.
+template <int FMT, int NP, bool SWIGLU>
 __global__ void __launch_bounds__(kGemvThreads, 3) qmm_gemv_kernel(const __grid_constant__ GemvArgs<NP> a) {
     namespace cg = cooperative_groups;
     constexpr int E = BlockTraits<FMT>::E;
@@ -95,14 +100,17 @@ __global__ void __launch_bounds__(kGemvThreads, 3) qmm_gemv_kernel(const __grid_
         const int mid = (lo + hi + 1) >> 1;
         if (a.p[mid].cta0 <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
     }
-    const int pi = lo;
-    const GemvProb &p = a.p[pi];
-    const int local = (int)blockIdx.x - p.cta0;
-    const int rank = local % a.cl;
+    const int base = SWIGLU ? (lo & ~1) : lo;
+    const int local = (int)blockIdx.x - a.p[base].cta0;
+    const int rank = local % a.cl;              // rank in the cluster
     const int64_t g = local / a.cl;
+    const int ks = SWIGLU ? a.cl >> 1 : a.cl;   // CTAs splitting one row's K
+    const int role = SWIGLU ? rank / ks : 0;    // SWIGLU: 0 gate, 1 up
+    const int krank = rank % ks;
+    const GemvProb &p = a.p[base + role];
     // blocks of this CTA and of this warp
     const int span = kGemvWarps * p.nbw;
-    const int c0 = min(p.blocks, rank * span), c1 = min(p.blocks, c0 + span);
+    const int c0 = min(p.blocks, krank * span), c1 = min(p.blocks, c0 + span);
     const int w0 = min(c1, c0 + warp * p.nbw), w1 = min(c1, w0 + p.nbw);
     const uint8_t *grp = p.W + g * p.group_vecs * kVecBytes + lane * kVec;
 
@@ -135,15 +143,22 @@ __global__ void __launch_bounds__(kGemvThreads, 3) qmm_gemv_kernel(const __grid_
 #pragma unroll
         for (int w = 0; w < kGemvWarps; ++w) s += red[w * 32 + threadIdx.x];
         red[threadIdx.x] = s;
-        if (a.cl == 1 && n < p.N) p.y[n] = s;
+        if (!SWIGLU && a.cl == 1 && n < p.N) p.y[n] = s;
     }
-    if (a.cl == 1) return;
+    if (!SWIGLU && a.cl == 1) return;
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     if (rank == 0 && threadIdx.x < 32) {
-        float s = red[threadIdx.x];
-        for (int r = 1; r < a.cl; ++r) s += cluster.map_shared_rank(red, r)[threadIdx.x];
-        if (n < p.N) p.y[n] = s;
+        if (!SWIGLU) {
+            float s = red[threadIdx.x];
+            for (int r = 1; r < a.cl; ++r) s += cluster.map_shared_rank(red, r)[threadIdx.x];
+            if (n < p.N) p.y[n] = s;
+        } else {
+            float gs = red[threadIdx.x], us = 0.f;
+            for (int r = 1; r < ks; ++r) gs += cluster.map_shared_rank(red, r)[threadIdx.x];
+            for (int r = ks; r < a.cl; ++r) us += cluster.map_shared_rank(red, r)[threadIdx.x];
+            if (n < p.N) p.y[n] = gs / (1.f + expf(-gs)) * us;  // silu(g) * u
+        }
     }
     cluster.sync();  // no CTA leaves while rank 0 reads its shared memory
 }

@@ -35,6 +35,7 @@ SIGNATURES = {
     "lean_unpack_canonical": (_int, [_int, _vp, _vp, _i64, _i64]),
     "lean_dequant": (_int, [_int, _vp, _vp, _i64, _i64, _vp]),
     "lean_embed_rows": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "lean_qmatmul_swiglu": (_int, [_int, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_uint, _vp]),
     "lean_qmatmul": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "lean_qmatmul_ex": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp]),
     "lean_qmatmul_workspace_bytes": (_i64, [_int, _i64, _i64, _i64]),
@@ -169,6 +170,14 @@ def lean_embed_rows(fmt: int, W_packed_dev, ids_dev, out_dev, n_ids: int, N: int
     """out[i][k] = w[ids[i]][k] (an embedding lookup); ids: int32 device tensor."""
     _check("lean_embed_rows", _lib.lean_embed_rows(fmt, _addr(W_packed_dev), _addr(ids_dev),
                                                    _addr(out_dev), n_ids, N, K, _stream(stream)))
+
+
+def lean_qmatmul_swiglu(fmt: int, W_gate_dev, W_up_dev, x_dev, h_dev, N: int, K: int,
+                        flags: int = 0, stream=None) -> None:
+    """h = silu(W_gate x) * (W_up x) in one launch (M = 1)."""
+    _check("lean_qmatmul_swiglu", _lib.lean_qmatmul_swiglu(
+        fmt, _addr(W_gate_dev), _addr(W_up_dev), _addr(x_dev), _addr(h_dev), N, K, flags,
+        _stream(stream)))
 
 
 def lean_qmatmul(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,

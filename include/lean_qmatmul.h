@@ -199,6 +199,27 @@ lean_status lean_qmatmul_ex(int fmt, const void *W_packed_dev, const float *x_de
                             float *y_dev, int64_t N, int64_t K, int64_t M,
                             unsigned flags, void *stream);
 
+/* The fused gate / up projections of a decode layer's FFN, with their
+ * epilogue: h[n] = silu(g[n]) * u[n], g = W_gate x, u = W_up x (M = 1),
+ * silu(t) = t / (1 + e^-t).  A decode step is N x (attention + FFN) ("wgpu-llm"
+ * README, Architecture at a Glance) and the FFN of the models the pages run
+ * (SmolLM2, Qwen2.5, TinyLlama) feeds its down projection with silu(gate) *
+ * up; this call reads x once per row group for both matrices, never stores
+ * g or u, and writes the down projection's input directly, in one launch.
+ *   W_gate_dev, W_up_dev  device, 16-byte aligned, both N x K of format fmt,
+ *                         packed by lean_pack
+ *   x_dev                 device, 16-byte aligned, x[K] fp32
+ *   h_dev                 device, 4-byte aligned, h[N] fp32, overwritten; must not
+ *                         overlap x or the weights
+ *   flags                 0 or LEAN_FLAG_EARLY_WEIGHTS (others: LEAN_ERR_FORMAT)
+ * Accuracy: g and u as lean_qmatmul's; h = fl(silu(g~)) * u~ in fp32.
+ * LEAN_ERR_SHAPE for K beyond 4 x 8 x (8 Q4_0, 4 Q8_0, 2 INT8-B64, 1 Q6_K)
+ * blocks (Q4_0 and Q6_K 8192, the int8 formats 4096), besides the usual shape
+ * and pointer errors.  Nothing is allocated. */
+lean_status lean_qmatmul_swiglu(int fmt, const void *W_gate_dev, const void *W_up_dev,
+                                const float *x_dev, float *h_dev, int64_t N, int64_t K,
+                                unsigned flags, void *stream);
+
 /* Rows of x from which lean_qmatmul uses the tensor cores (16). */
 int lean_tensor_core_min_m(void);
 
