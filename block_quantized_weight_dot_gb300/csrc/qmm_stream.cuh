@@ -164,9 +164,10 @@ struct StreamRing<Q4_0, true> {
 // x as integer planes (dp4a) for the integer formats
 template <int FMT> struct XPlanes { static constexpr bool on = FMT != Q6_K; };
 // One 32-element block of x in plane form: a 32-byte header {init3, init2,
-// init1, init0, scale, fine, 0, 0} (scale = 2^-s, times 1/16 for Q4_0; -1
-// marks a block that takes the exact fp32 dot; fine = 0: the lowest plane is
-// all zero), then planes 3 (the top digits), 2, 1 and 0, 32 signed bytes each.
+// init1, init0 (the scale in chunks of tier 0 or 3), scale, tier of the
+// chunk, 0, 0} (scale = 2^-sf, 1/16 more for Q4_0; -1 marks a block that takes
+// the exact fp32 dot), then planes 3 (the top digits), 2, 1 and 0, 32 bytes
+// each.
 constexpr int kXqBytes = kXqBlockBytes;
 constexpr int kXqHeader = 32;
 static_assert(kXqBytes == kXqHeader + 4 * 32, "header + four planes");
@@ -342,7 +343,7 @@ __device__ __forceinline__ void x_block_store_int8(float v, uint8_t *dst, int la
     if (lane == 0) {
         const float scale = mx >= 0x7f800000u ? __int_as_float(0x7fc00000)
                                               : (FMT == Q4_0 ? s * (1.f / 16.f) : s);
-        reinterpret_cast<int4 *>(dst)[0] = make_int4(-128 * sq, 0, 0, 0);
+        reinterpret_cast<int4 *>(dst)[0] = make_int4(-128 * sq, 0, 0, __float_as_int(scale));
         reinterpret_cast<int4 *>(dst)[1] = make_int4(__float_as_int(scale), 3, 0, 0);
     }
 }
@@ -367,7 +368,11 @@ __device__ __forceinline__ void x_block_store(const XBlock &xb, int mode, uint8_
         // place as 16 * q): its scale carries the 1/16
         const int sc = xb.sf + (FMT == Q4_0 ? 4 : 0);
         const float scale = xb.tier == 2 ? -1.f : __int_as_float((127 - sc) << 23);
-        reinterpret_cast<int4 *>(dst)[0] = make_int4(-128 * s3, -128 * s2, -128 * s1, -128 * s0);
+        // chunks of tier 0 need no init of the lowest plane (all zero): its
+        // slot carries the scale, times 256 (their sums come out as T / 256),
+        // so that one load brings the whole header
+        const int w = mode == 0 ? __float_as_int(scale * 256.f) : -128 * s0;
+        reinterpret_cast<int4 *>(dst)[0] = make_int4(-128 * s3, -128 * s2, -128 * s1, w);
         reinterpret_cast<int4 *>(dst)[1] = make_int4(__float_as_int(scale), mode, 0, 0);
     }
 }
@@ -451,10 +456,9 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
 // x as int8 codes, in the top plane alone.  Returns the block's exact sum of
 // (weight byte - offset) * X (times 16 for Q4_0), rounded once to fp32.
 template <bool LO16, int TIER>
-__device__ __forceinline__ float plane_dot(const uint32_t (&w)[8], const uint8_t *xq) {
+__device__ __forceinline__ float plane_dot(const uint32_t (&w)[8], const int4 &h, const uint8_t *xq) {
     constexpr bool FINE = TIER == 1;
     constexpr int L = LO16 ? 16 : 1;
-    const int4 h = *reinterpret_cast<const int4 *>(xq);
     const uint4 *pl = reinterpret_cast<const uint4 *>(xq + kXqHeader);
     const uint4 a3 = pl[0], b3 = pl[1];
     const uint32_t P3[8] = {a3.x, a3.y, a3.z, a3.w, b3.x, b3.y, b3.z, b3.w};
@@ -492,7 +496,14 @@ __device__ __forceinline__ float plane_dot(const uint32_t (&w)[8], const uint8_t
         }
     }
     const int u3 = (int)s3 * L + (int)t3, u2 = (int)s2 * L + (int)t2, u1 = (int)s1 * L + (int)t1;
-    const int u0 = FINE ? (int)s0 * L + (int)t0 : 0;
+    if (!FINE) {
+        // the lowest plane is zero: T / 256 = (u3 * 256 + u2) * 256 + u1, with
+        // |u1| < 2^21 exact in fp32 and no cancellation against the first
+        // term once that one rounds (|u3 * 256 + u2| >= 2^24); one FMA rounds
+        // the rest (the tier's scale carries the factor 256)
+        return fmaf((float)(u3 * 256 + u2), 256.f, (float)u1);
+    }
+    const int u0 = (int)s0 * L + (int)t0;
     // |u| < 2^21, so both halves are exact in int32.  T = hi * 2^16 + lo is
     // rewritten as hi' * 2^16 + lo' with lo' = lo mod 2^16 in 0..65535 (the
     // carry moves into hi'): the FMA then rounds once, without cancellation,
@@ -537,11 +548,14 @@ __device__ __noinline__ float exact_block_dot(uint4 wa, uint4 wb, float d, const
 template <int FMT, int MODE>
 __device__ __forceinline__ float x_block_dot(const uint32_t (&w)[8], float d, const uint8_t *xq,
                                              const float *xg) {
-    const float scale = *reinterpret_cast<const float *>(xq + 16);
+    const int4 h = *reinterpret_cast<const int4 *>(xq);
+    // tiers 0 and 3 carry the scale in the header's last slot
+    const float scale = (MODE == 0 || MODE == 3) ? __int_as_float(h.w)
+                                                 : *reinterpret_cast<const float *>(xq + 16);
     if (MODE == 2 && scale < 0.f)
         return exact_block_dot<FMT>(make_uint4(w[0], w[1], w[2], w[3]),
                                     make_uint4(w[4], w[5], w[6], w[7]), d, xg);
-    return (d * scale) * plane_dot<FMT == Q4_0, MODE == 2 ? 1 : MODE>(w, xq);
+    return (d * scale) * plane_dot<FMT == Q4_0, MODE == 2 ? 1 : MODE>(w, h, xq);
 }
 // One block with x as planes: this lane's row, block b of the step at ws, x
 // planes of the chunk at xq, fp32 x of the chunk at xg.
