@@ -62,6 +62,10 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
 // M = 1 on the one-wave kernel; *done = false when the problems do not fit it
 template <int FMT>
 lean_status gemv_fmt(const HostProb *ph, int n, unsigned flags, cudaStream_t stream, bool *done);
+// M = 2..16 on the one-wave kernel; *done = false when a row does not fit it
+template <int FMT>
+lean_status gemv_small_m_fmt(const HostProb &hp, int M, unsigned flags, cudaStream_t stream,
+                             bool *done);
 // h = silu(W_gate x) * (W_up x); ph[0] gate (its x and y are the call's), ph[1] up
 template <int FMT>
 lean_status swiglu_fmt(const HostProb *ph, unsigned flags, cudaStream_t stream);

@@ -297,7 +297,7 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
 
 // ------------------------------------------------------- one-wave M = 1 path ---
 
-// CTAs of qmm_gemv_kernel<FMT, NP> resident per SM (read once per device).
+// CTAs of qmm_gemv_kernel<FMT, NP, false, 1> resident per SM (read once per device).
 template <int FMT, int NP>
 inline int gemv_ctas_per_sm() {
     static std::atomic<int> cache[kMaxDevices];
@@ -305,9 +305,9 @@ inline int gemv_ctas_per_sm() {
     if (dev < 0) return 0;
     int v = cache[dev].load(std::memory_order_relaxed);
     if (v == 0) {
-        constexpr int smem = (kGemvWarps * GemvCfg<FMT>::NB * BlockTraits<FMT>::E + 256) * 4;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, qmm_gemv_kernel<FMT, NP, false>,
-                                                          kGemvThreads, smem) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, qmm_gemv_kernel<FMT, NP, false, 1>,
+                                                          kGemvThreads,
+                                                          gemv_smem_bytes<FMT, 1>()) != cudaSuccess ||
             v <= 0)
             v = -1;
         cache[dev].store(v, std::memory_order_relaxed);
@@ -315,75 +315,46 @@ inline int gemv_ctas_per_sm() {
     return v;
 }
 
-// The product on qmm_gemv_kernel when every problem fits it and the whole
-// grid fits the GPU at once; *done = false leaves the call to the stream path.
-template <int FMT, int NP>
-lean_status launch_gemv(const HostProb *ph, int n, unsigned flags, cudaStream_t stream,
-                        bool *done) {
-    constexpr int NB = GemvCfg<FMT>::NB;
+// The product on qmm_gemv_kernel for MT rows of x (M <= MT) when every
+// problem's row fits a cluster of 8 CTAs; with one_wave, only when the whole
+// grid also fits the GPU at once.  *done = false leaves the call to the other
+// kernels.  SWIGLU: ph[0] gate, ph[1] up (n = 2), h = silu(g) * u.
+template <int FMT, int NP, int MT, bool SWIGLU>
+lean_status launch_gemv(const HostProb *ph, int n, int M, unsigned flags, bool one_wave,
+                        cudaStream_t stream, bool *done) {
+    constexpr int NB = gemv_nb<FMT, MT>();
+    static std::atomic<uint64_t> smem_done{0};
     *done = false;
-    // the smallest cluster for which every row's blocks fit 8 warps x NB
     int64_t maxb = 0, groups = 0;
     for (int i = 0; i < n; ++i) {
         maxb = std::max<int64_t>(maxb, ph[i].g.blocks);
         groups += ph[i].g.groups;
     }
-    const int cl = (int)((maxb + kGemvWarps * NB - 1) / (kGemvWarps * NB));
-    if (cl > kGemvMaxCluster) return LEAN_OK;
-    const int per_sm = gemv_ctas_per_sm<FMT, NP>();
-    if (per_sm <= 0 || groups * cl > (int64_t)per_sm * sm_count()) return LEAN_OK;
+    if (SWIGLU) groups = ph[0].g.groups;
+    // the smallest K split for which every row's blocks fit 8 warps x NB
+    const int ks = (int)((maxb + kGemvWarps * NB - 1) / (kGemvWarps * NB));
+    const int cl = SWIGLU ? 2 * ks : ks;
+    if (cl > kGemvMaxCluster) return SWIGLU ? LEAN_ERR_SHAPE : LEAN_OK;
+    if (groups * cl > INT32_MAX) return LEAN_ERR_SHAPE;
+    if (one_wave) {
+        const int per_sm = gemv_ctas_per_sm<FMT, NP>();
+        if (per_sm <= 0 || groups * cl > (int64_t)per_sm * sm_count()) return LEAN_OK;
+    }
+    auto kern = qmm_gemv_kernel<FMT, NP, SWIGLU, MT>;
+    if (!ensure_smem(kern, (size_t)gemv_smem_bytes<FMT, MT>(), smem_done)) return LEAN_ERR_CUDA;
     GemvArgs<NP> a;
     a.nprob = n;
     a.cl = cl;
+    a.M = M;
+    a.pad = 0;
     a.mg = make_magic();
     int cta = 0;
     for (int i = 0; i < n; ++i) {
         const Geom &g = ph[i].g;
         GemvProb &p = a.p[i];
         p.W = ph[i].W;
-        p.x = ph[i].x;
-        p.y = ph[i].y;
-        p.N = (int)g.N;
-        p.K = (int)g.K;
-        p.blocks = (int)g.blocks;
-        p.steps = g.steps;
-        p.last_blocks = g.last_blocks;
-        p.step_vecs = g.step_vecs;
-        p.nbw = (int)((g.blocks + kGemvWarps * cl - 1) / (kGemvWarps * cl));
-        p.cta0 = cta;
-        p.group_vecs = g.group_vecs;
-        cta += (int)g.groups * cl;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)cta, 1, 1);
-    cfg.blockDim = dim3(kGemvThreads, 1, 1);
-    cfg.dynamicSmemBytes = (kGemvWarps * NB * BlockTraits<FMT>::E + 256) * 4;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    fill_launch(cfg, attr, cl, flags);
-    *done = true;
-    return cudaLaunchKernelEx(&cfg, qmm_gemv_kernel<FMT, NP, false>, a) == cudaSuccess
-               ? LEAN_OK
-               : LEAN_ERR_CUDA;
-}
-
-// h = silu(W_gate x) * (W_up x) on the one-wave kernel (any number of waves):
-// a cluster of 2 x (K split) CTAs per row group.  ph[0] gate, ph[1] up.
-template <int FMT>
-lean_status swiglu_fmt(const HostProb *ph, unsigned flags, cudaStream_t stream) {
-    constexpr int NB = GemvCfg<FMT>::NB;
-    const Geom &g = ph[0].g;
-    const int ks = (int)((g.blocks + kGemvWarps * NB - 1) / (kGemvWarps * NB));
-    if (2 * ks > kGemvMaxCluster || g.groups * 2 * ks > INT32_MAX) return LEAN_ERR_SHAPE;
-    GemvArgs<2> a;
-    a.nprob = 2;
-    a.cl = 2 * ks;
-    a.mg = make_magic();
-    for (int i = 0; i < 2; ++i) {
-        GemvProb &p = a.p[i];
-        p.W = ph[i].W;
-        p.x = ph[0].x;
-        p.y = ph[0].y;
+        p.x = SWIGLU ? ph[0].x : ph[i].x;
+        p.y = SWIGLU ? ph[0].y : ph[i].y;
         p.N = (int)g.N;
         p.K = (int)g.K;
         p.blocks = (int)g.blocks;
@@ -391,26 +362,51 @@ lean_status swiglu_fmt(const HostProb *ph, unsigned flags, cudaStream_t stream) 
         p.last_blocks = g.last_blocks;
         p.step_vecs = g.step_vecs;
         p.nbw = (int)((g.blocks + kGemvWarps * ks - 1) / (kGemvWarps * ks));
-        p.cta0 = 0;
+        p.cta0 = cta;
         p.group_vecs = g.group_vecs;
+        if (!SWIGLU) cta += (int)g.groups * cl;
     }
+    if (SWIGLU) cta = (int)groups * cl;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(g.groups * 2 * ks), 1, 1);
+    cfg.gridDim = dim3((unsigned)cta, 1, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
-    cfg.dynamicSmemBytes = (kGemvWarps * NB * BlockTraits<FMT>::E + 256) * 4;
+    cfg.dynamicSmemBytes = gemv_smem_bytes<FMT, MT>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
-    fill_launch(cfg, attr, 2 * ks, flags);
-    return cudaLaunchKernelEx(&cfg, qmm_gemv_kernel<FMT, 2, true>, a) == cudaSuccess
-               ? LEAN_OK
-               : LEAN_ERR_CUDA;
+    fill_launch(cfg, attr, cl, flags);
+    *done = true;
+    return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
 }
 
+// h = silu(W_gate x) * (W_up x) on the one-wave kernel (any number of waves):
+// a cluster of 2 x (K split) CTAs per row group.  ph[0] gate, ph[1] up.
+template <int FMT>
+lean_status swiglu_fmt(const HostProb *ph, unsigned flags, cudaStream_t stream) {
+    bool done = false;
+    return launch_gemv<FMT, 2, 1, true>(ph, 2, 1, flags, false, stream, &done);
+}
+
+// M = 1: the one-wave kernel when the grid fits the GPU at once.
 template <int FMT>
 lean_status gemv_fmt(const HostProb *ph, int n, unsigned flags, cudaStream_t stream, bool *done) {
-    if (n == 1) return launch_gemv<FMT, 1>(ph, n, flags, stream, done);
-    if (n <= 8) return launch_gemv<FMT, 8>(ph, n, flags, stream, done);
-    return launch_gemv<FMT, kMaxBatch>(ph, n, flags, stream, done);
+    if (n == 1) return launch_gemv<FMT, 1, 1, false>(ph, n, 1, flags, true, stream, done);
+    if (n <= 8) return launch_gemv<FMT, 8, 1, false>(ph, n, 1, flags, true, stream, done);
+    return launch_gemv<FMT, kMaxBatch, 1, false>(ph, n, 1, flags, true, stream, done);
+}
+
+// M = 2..16 rows of x on the same kernel (several waves allowed) when a row
+// fits a cluster; *done = false leaves the call to the CUDA-core kernel.
+template <int FMT>
+lean_status gemv_small_m_fmt(const HostProb &hp, int M, unsigned flags, cudaStream_t stream,
+                             bool *done) {
+    if (M <= 2) return launch_gemv<FMT, 1, 2, false>(&hp, 1, M, flags, false, stream, done);
+    if (M <= 4) return launch_gemv<FMT, 1, 4, false>(&hp, 1, M, flags, false, stream, done);
+    if (FMT == Q6_K) {  // its x slice would not fit for 8 rows or more
+        *done = false;
+        return LEAN_OK;
+    }
+    if (M <= 8) return launch_gemv<FMT, 1, 8, false>(&hp, 1, M, flags, false, stream, done);
+    return launch_gemv<FMT, 1, 16, false>(&hp, 1, M, flags, false, stream, done);
 }
 
 // -------------------------------------------------------------- stream path ---
@@ -621,6 +617,8 @@ lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int6
                                          bool, unsigned *, cudaStream_t);                      \
     template lean_status gemv_fmt<FMT>(const HostProb *, int, unsigned, cudaStream_t, bool *); \
     template lean_status swiglu_fmt<FMT>(const HostProb *, unsigned, cudaStream_t);              \
+    template lean_status gemv_small_m_fmt<FMT>(const HostProb &, int, unsigned, cudaStream_t,    \
+                                               bool *);                                           \
     template lean_status mma_fmt<FMT>(const Geom &, const uint8_t *, const float *, float *,   \
                                       int64_t, unsigned, void *, int64_t, unsigned *,          \
                                       cudaStream_t);

@@ -172,6 +172,20 @@ lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_de
         }
         return LEAN_ERR_FORMAT;
     }
+    {  // 2..15 rows: the one-wave kernel when a row fits a cluster of it
+        HostProb hp = {W, x_dev, y_dev, g};
+        bool done = false;
+        lean_status st2 = LEAN_OK;
+        if (!(flags & LEAN_FLAG_STREAM)) {
+            switch (fmt) {
+            case LEAN_Q4_0: st2 = gemv_small_m_fmt<Q4_0>(hp, (int)M, flags, s, &done); break;
+            case LEAN_Q8_0: st2 = gemv_small_m_fmt<Q8_0>(hp, (int)M, flags, s, &done); break;
+            case LEAN_I8_B64: st2 = gemv_small_m_fmt<I8_B64>(hp, (int)M, flags, s, &done); break;
+            case LEAN_Q6_K: st2 = gemv_small_m_fmt<Q6_K>(hp, (int)M, flags, s, &done); break;
+            }
+        }
+        if (done || st2 != LEAN_OK) return st2;
+    }
     switch (fmt) {
     case LEAN_Q4_0: return simt_fmt<Q4_0>(g, W, x_dev, y_dev, M, flags, s);
     case LEAN_Q8_0: return simt_fmt<Q8_0>(g, W, x_dev, y_dev, M, flags, s);

@@ -36,12 +36,25 @@ constexpr int kGemvThreads = 32 * kGemvWarps;
 constexpr int kGemvMaxCluster = 8;
 
 // Blocks a lane holds in registers at most (four 16-byte vectors per block of
-// the int8 formats: Q8_0 2, I8_B64 4; Q6_K 13 vectors).
+// the int8 formats: Q8_0 2, I8_B64 4; Q6_K 13 vectors), for MT rows of x: with
+// 8 or 16 rows fewer, so that the CTA's x slice stays within 32 KB.
 template <int FMT> struct GemvCfg;
 template <> struct GemvCfg<Q4_0> { static constexpr int NB = 8; };
 template <> struct GemvCfg<Q8_0> { static constexpr int NB = 4; };
 template <> struct GemvCfg<I8_B64> { static constexpr int NB = 2; };
 template <> struct GemvCfg<Q6_K> { static constexpr int NB = 1; };
+template <int FMT, int MT>
+constexpr int gemv_nb() {
+    return MT <= 4 ? GemvCfg<FMT>::NB
+                   : (GemvCfg<FMT>::NB * 4 / MT > 0 ? GemvCfg<FMT>::NB * 4 / MT : 1);
+}
+// floats of x one CTA stages per row of x
+template <int FMT, int MT>
+constexpr int gemv_xstride() { return kGemvWarps * gemv_nb<FMT, MT>() * BlockTraits<FMT>::E; }
+template <int FMT, int MT>
+constexpr int gemv_smem_bytes() {
+    return (MT * gemv_xstride<FMT, MT>() + kGemvWarps * MT * 32) * 4;
+}
 
 struct GemvProb {
     const uint8_t *W;
@@ -59,6 +72,8 @@ template <int NP>
 struct GemvArgs {
     int nprob;
     int cl;  // CTAs per cluster (K split), the same for every problem
+    int M;   // rows of x (<= MT of the kernel); x[M][K], y[M][N]
+    int pad;
     Magic mg;
     GemvProb p[NP];
 };
@@ -80,18 +95,22 @@ __device__ __forceinline__ void gemv_load(BlockFrag<FMT> &f, const GemvProb &p, 
 }
 
 // grid.x = sum over problems of groups * cl; cluster = (cl, 1, 1);
-// blockDim.x = 256; dynamic shared memory: the CTA's x slice (8 * nbw * E
-// floats of the largest problem) then 8 x 32 partial sums.
-// SWIGLU: the problems come in pairs (gate, up) of one shape, x and output;
-// each row group gets a cluster of cl = 2 * (K split) CTAs, the first half on
-// the gate rows, the second on the up rows, and rank 0 writes
+// blockDim.x = 256; dynamic shared memory gemv_smem_bytes<FMT, MT>(): the
+// CTA's slice of each of the MT rows of x, then 8 x MT x 32 partial sums.
+// MT > 1: the same for up to MT rows of x, each decoded weight multiplied into
+// all of them (x rows past M read as zero).
+// SWIGLU (MT = 1): the problems come in pairs (gate, up) of one shape, x and
+// output; each row group gets a cluster of cl = 2 * (K split) CTAs, the first
+// half on the gate rows, the second on the up rows, and rank 0 writes
 // h = silu(gate . x) * (up . x) (the input of the FFN's down projection).
 // A pair's two entries carry the same cta0.
-template <int FMT, int NP, bool SWIGLU>
-__global__ void __launch_bounds__(kGemvThreads, 3) qmm_gemv_kernel(const __grid_constant__ GemvArgs<NP> a) {
+template <int FMT, int NP, bool SWIGLU, int MT>
+__global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
+    qmm_gemv_kernel(const __grid_constant__ GemvArgs<NP> a) {
     namespace cg = cooperative_groups;
     constexpr int E = BlockTraits<FMT>::E;
-    constexpr int NB = GemvCfg<FMT>::NB;
+    constexpr int NB = gemv_nb<FMT, MT>();
+    constexpr int XS = gemv_xstride<FMT, MT>();
     extern __shared__ __align__(16) float gsm[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // this CTA's problem: the last one whose first CTA is at or before it
@@ -123,41 +142,54 @@ __global__ void __launch_bounds__(kGemvThreads, 3) qmm_gemv_kernel(const __grid_
     pdl_wait();  // x may come from the previous kernel on the stream
 
     float *xs = gsm;
-    const float4 *src = reinterpret_cast<const float4 *>(p.x + (int64_t)c0 * E);
-    for (int i = threadIdx.x; i < (c1 - c0) * (E / 4); i += kGemvThreads)
-        reinterpret_cast<float4 *>(xs)[i] = src[i];
+    const int nv = (c1 - c0) * (E / 4);  // float4 per row of the slice
+    for (int i = threadIdx.x; i < MT * nv; i += kGemvThreads) {
+        const int m = i / nv, v = i % nv;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m < a.M)
+            val = reinterpret_cast<const float4 *>(p.x + (int64_t)m * p.K + (int64_t)c0 * E)[v];
+        reinterpret_cast<float4 *>(xs + m * XS)[v] = val;
+    }
     __syncthreads();
 
-    float tot[1] = {0.f};
+    float tot[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) tot[m] = 0.f;
 #pragma unroll
     for (int i = 0; i < NB; ++i)
-        if (w0 + i < w1) block_fma<FMT, 1>(f[i], xs + (w0 + i - c0) * E, 0, mg, tot);
+        if (w0 + i < w1) block_fma<FMT, MT>(f[i], xs + (w0 + i - c0) * E, XS, mg, tot);
 
     // the 8 warps' sums, then (cluster) the CTAs' sums, each in a fixed order
-    float *red = gsm + kGemvWarps * GemvCfg<FMT>::NB * E;
-    red[warp * 32 + lane] = tot[0];
+    float *red = gsm + MT * XS;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) red[(warp * MT + m) * 32 + lane] = tot[m];
     __syncthreads();
-    const int64_t n = g * kRowsPerGroup + threadIdx.x;
-    if (threadIdx.x < 32) {
+    for (int i = threadIdx.x; i < MT * 32; i += kGemvThreads) {
         float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < kGemvWarps; ++w) s += red[w * 32 + threadIdx.x];
-        red[threadIdx.x] = s;
-        if (!SWIGLU && a.cl == 1 && n < p.N) p.y[n] = s;
+        for (int w = 0; w < kGemvWarps; ++w) s += red[w * MT * 32 + i];
+        red[i] = s;  // warp 0's slots: row m = i / 32, lane i % 32
+        const int m = i >> 5;
+        const int64_t n = g * kRowsPerGroup + (i & 31);
+        if (!SWIGLU && a.cl == 1 && m < a.M && n < p.N) p.y[(int64_t)m * p.N + n] = s;
     }
     if (!SWIGLU && a.cl == 1) return;
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    if (rank == 0 && threadIdx.x < 32) {
-        if (!SWIGLU) {
-            float s = red[threadIdx.x];
-            for (int r = 1; r < a.cl; ++r) s += cluster.map_shared_rank(red, r)[threadIdx.x];
-            if (n < p.N) p.y[n] = s;
-        } else {
-            float gs = red[threadIdx.x], us = 0.f;
-            for (int r = 1; r < ks; ++r) gs += cluster.map_shared_rank(red, r)[threadIdx.x];
-            for (int r = ks; r < a.cl; ++r) us += cluster.map_shared_rank(red, r)[threadIdx.x];
-            if (n < p.N) p.y[n] = gs / (1.f + expf(-gs)) * us;  // silu(g) * u
+    if (rank == 0) {
+        for (int i = threadIdx.x; i < MT * 32; i += kGemvThreads) {
+            const int m = i >> 5;
+            const int64_t n = g * kRowsPerGroup + (i & 31);
+            if (!SWIGLU) {
+                float s = red[i];
+                for (int r = 1; r < a.cl; ++r) s += cluster.map_shared_rank(red, r)[i];
+                if (m < a.M && n < p.N) p.y[(int64_t)m * p.N + n] = s;
+            } else {
+                float gs = red[i], us = 0.f;
+                for (int r = 1; r < ks; ++r) gs += cluster.map_shared_rank(red, r)[i];
+                for (int r = ks; r < a.cl; ++r) us += cluster.map_shared_rank(red, r)[i];
+                if (n < p.N) p.y[n] = gs / (1.f + expf(-gs)) * us;  // silu(g) * u
+            }
         }
     }
     cluster.sync();  // no CTA leaves while rank 0 reads its shared memory
