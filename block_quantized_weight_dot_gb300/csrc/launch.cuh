@@ -12,6 +12,7 @@
 #include "layout.h"
 #include "qmm_gemv.cuh"
 #include "qmm_mma.cuh"
+#include "qmm_mma_wide.cuh"
 #include "qmm_simt.cuh"
 #include "qmm_stream.cuh"
 
@@ -215,10 +216,94 @@ inline int mma_split(int64_t tiles, int nsl, int64_t slots) {
     return ks;
 }
 
+// The tensor-core product for more than 64 rows of x (qmm_mma_wide.cuh):
+// weights split on the CUDA cores, 256-row tiles of x.
+template <int FMT>
+lean_status mma_wide_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
+                    unsigned flags, void *ws, int64_t ws_bytes, unsigned *err,
+                    cudaStream_t stream) {
+    static std::atomic<uint64_t> smem_done{0}, smem_done_x{0};
+    const int64_t tiles = (g.N + wide::kMmaRows - 1) / wide::kMmaRows;
+    const int nkb = (int)((g.K + wide::kMmaKB - 1) / wide::kMmaKB);
+    const int nsl = (nkb + wide::kMmaSub - 1) / wide::kMmaSub;
+    const int64_t mtiles = (M + wide::kMmaMaxN - 1) / wide::kMmaMaxN;
+    const int mpad = ((int)std::min<int64_t>(M, wide::kMmaMaxN) + 15) & ~15;
+    const int RS = wide::mma_raw_slots<FMT>(mpad);
+    const size_t smem = (size_t)wide::mma_smem_bytes<FMT>(mpad, RS);
+    // one CTA per SM: the rings take most of the shared memory and all 512
+    // tensor-memory columns are allocated
+    const int ks = mma_split(tiles * mtiles, nsl, (int64_t)sm_count());
+    if (tiles * ks > INT32_MAX || RS < 1) return LEAN_ERR_SHAPE;
+    const int64_t xs_bytes = wide::mma_xs_bytes(M, g.K);
+    if (ws && ws_bytes < xs_bytes) return LEAN_ERR_SHAPE;
+    uint8_t *xs = static_cast<uint8_t *>(ws);
+    wide::MmaArgs a = {};
+    a.W = W;
+    a.x = x;
+    a.xs = xs;
+    a.y = y;
+    a.N = (int)g.N;
+    a.K = (int)g.K;
+    a.M = (int)M;
+    a.ks = ks;
+    a.nkb = nkb;
+    a.nsl = nsl;
+    a.RS = RS;
+    a.BS = wide::mma_b_stages(mpad);
+    a.raw_off = wide::mma_raw_off(mpad);
+    a.groups = g.groups;
+    a.steps = g.steps;
+    a.last_blocks = g.last_blocks;
+    a.step_vecs = g.step_vecs;
+    a.group_vecs = g.group_vecs;
+    a.err = err;
+    a.mg = make_magic();
+    if (xs) {
+        // x -> bf16 hi / lo operand tiles, once
+        wide::XsplitArgs xa;
+        xa.x = x;
+        xa.xs = xs;
+        xa.M = (int)M;
+        xa.K = (int)g.K;
+        xa.nkb = nkb;
+        xa.mtiles = (int)mtiles;
+        xa.rows = (mtiles - 1) * wide::kMmaMaxN + (((M - (mtiles - 1) * wide::kMmaMaxN) + 15) & ~15);
+        const int64_t blocks = (xa.rows * nkb * 8 + 255) / 256;
+        if (blocks > INT32_MAX) return LEAN_ERR_SHAPE;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        fill_launch(cfg, attr, 1, flags);
+        if (cudaLaunchKernelEx(&cfg, wide::xsplit_kernel, xa) != cudaSuccess) return LEAN_ERR_CUDA;
+    }
+    auto kern = xs ? wide::qmm_mma_kernel<FMT, true> : wide::qmm_mma_kernel<FMT, false>;
+    std::atomic<uint64_t> &sd = xs ? smem_done : smem_done_x;
+    if (!ensure_smem(kern, (size_t)wide::kMmaSmemLimit, sd)) return LEAN_ERR_CUDA;
+    for (int64_t t0 = 0; t0 < mtiles; t0 += 65535) {
+        a.m_base = (int)(t0 * wide::kMmaMaxN);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim =
+            dim3((unsigned)(tiles * ks), (unsigned)std::min<int64_t>(65535, mtiles - t0), 1);
+        cfg.blockDim = dim3(wide::kMmaThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        // after the split kernel (which itself starts only when the caller's
+        // flags allow) the launch is always programmatic
+        fill_launch(cfg, attr, ks, xs ? (unsigned)LEAN_FLAG_EARLY_WEIGHTS : flags);
+        if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return LEAN_ERR_CUDA;
+    }
+    return LEAN_OK;
+}
+
 template <int FMT>
 lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
                     unsigned flags, void *ws, int64_t ws_bytes, unsigned *err,
                     cudaStream_t stream) {
+    // more than one 64-row tile of x: one weight conversion per 256 rows
+    if (M > kMmaMaxN) return mma_wide_fmt<FMT>(g, W, x, y, M, flags, ws, ws_bytes, err, stream);
     static std::atomic<uint64_t> smem_done{0}, smem_done_x{0};
     const int64_t tiles = (g.N + kMmaRows - 1) / kMmaRows;
     const int nkb = (int)((g.K + kMmaKB - 1) / kMmaKB);
@@ -246,7 +331,6 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
     a.nkb = nkb;
     a.nsl = nsl;
     a.RS = RS;
-    a.BS = mma_b_stages(mpad);
     a.raw_off = mma_raw_off(mpad);
     a.groups = g.groups;
     a.steps = g.steps;

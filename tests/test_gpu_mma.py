@@ -1,10 +1,12 @@
-"""GPU parity of the tensor-core product (16 or more rows of x): split-bf16
-tcgen05 MMAs against the fp64 oracle.
+"""GPU parity of the tensor-core products (16 or more rows of x) against the
+fp64 oracle: up to 64 rows, integer codes times split-bf16 x with the block
+scales applied per group after the MMAs; more rows, split-bf16 weights times
+split-bf16 x in 256-row tiles of x.
 
 Covers ragged row tiles (N not a multiple of 128), K tails (K not a multiple
-of 64), K split over a thread-block cluster (few row tiles, long K), several
-256-row tiles of x with a ragged last one, the switch-over from the CUDA-core
-path at 16 rows, bit-exact one-hot products for Q4_0 (whose split is exact),
+of 64), K split over a thread-block cluster (few row tiles, long K), x tiles
+with a ragged last one (both kernels), the switch-over from the CUDA-core
+path at 16 rows, bit-exact one-hot products for Q4_0 (exact in both),
 determinism, writes confined to y, and the device error word left clear --
 each both with a caller workspace (x split once by its own kernel) and
 without one (each CTA splits its x).
