@@ -610,15 +610,22 @@ def linear_path(lin, tc_min):
 
 
 def mma_issued_flops(lin):
-    """bf16 MMA work the tensor-core kernel issues for one product: three MMAs
-    (w_hi x_hi, w_hi x_lo, w_lo x_hi) per 16-wide K step for every 128-row
-    weight tile against the tile's rows of x padded to 16, K padded to 64."""
+    """bf16 MMA work the tensor-core kernels issue for one product, for every
+    128-row weight tile and K padded to 64.  Up to 64 rows of x: the integer
+    codes times x_hi and x_lo (two MMAs per 16-wide K step; Q6_K's codes in two
+    parts, three), x rows padded to 16.  More rows: split weights times split
+    x (three MMAs per step) in 256-row tiles of x, each padded to 16."""
     kp = -(-lin.K // 64) * 64
     tiles = -(-lin.N // 128)
-    mp = 0
-    for m0 in range(0, lin.M, 256):
-        mp += -(-min(256, lin.M - m0) // 16) * 16
-    return 3 * 2 * 128 * tiles * mp * kp
+    if lin.M <= 64:
+        per_step = 3 if lin.fmt == syn.Q6_K else 2
+        mp = -(-lin.M // 16) * 16
+    else:
+        per_step = 3
+        mp = 0
+        for m0 in range(0, lin.M, 256):
+            mp += -(-min(256, lin.M - m0) // 16) * 16
+    return per_step * 2 * 128 * tiles * mp * kp
 
 
 def time_linear(lin, device, l2, stream, reps=20):
@@ -661,8 +668,9 @@ def time_linear(lin, device, l2, stream, reps=20):
         r["tensor_pipe"] = {"issued_bf16_TFLOP/s": round(issued, 1),
                             "frac_of_bf16_peak": round(issued / bf16_peak, 4),
                             "peak": bf16_peak, "peak_source": bf16_kind,
-                            "basis": "bf16 MMA work the kernel issues (3 MMAs per 16-wide K "
-                                     "step, x rows padded to 16, K to 64) over CUDA-event time"}
+                            "basis": "bf16 MMA work the kernels issue (per 16-wide K step 2 MMAs "
+                                     "up to 64 rows of x, Q6_K 3; 3 above 64 rows; x rows padded "
+                                     "to 16, K to 64) over CUDA-event time"}
     del dw, g
     torch.cuda.empty_cache()
     return r

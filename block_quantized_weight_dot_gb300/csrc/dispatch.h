@@ -74,6 +74,10 @@ template <int FMT>
 lean_status stream_fmt(const HostProb *ph, int n, unsigned flags, void *ws, int64_t ws_bytes,
                        bool planes, unsigned *err, cudaStream_t stream);
 
+// Device address of the library's error word on the current device (looked up
+// once per device), or null.
+unsigned *error_word();
+
 // The M = 1 product with a workspace; planes = false keeps x in fp32 (the
 // layout without a plane region, as the fixed array of lean_qmatmul_fixed_ws).
 // clear_counters: once every argument has been checked, zero the arrival

@@ -130,6 +130,9 @@ inline SimtArgs simt_args(const Geom &g, const uint8_t *W, const float *x, float
     a.step_vecs = g.step_vecs;
     a.group_vecs = g.group_vecs;
     a.mg = make_magic();
+#ifdef LEAN_DEBUG
+    a.err = error_word();
+#endif
     return a;
 }
 
@@ -257,6 +260,7 @@ lean_status mma_wide_fmt(const Geom &g, const uint8_t *W, const float *x, float 
     a.step_vecs = g.step_vecs;
     a.group_vecs = g.group_vecs;
     a.err = err;
+    a.xs_bytes = xs ? xs_bytes : 0;
     a.mg = make_magic();
     if (xs) {
         // x -> bf16 hi / lo operand tiles, once
@@ -267,6 +271,8 @@ lean_status mma_wide_fmt(const Geom &g, const uint8_t *W, const float *x, float 
         xa.K = (int)g.K;
         xa.nkb = nkb;
         xa.mtiles = (int)mtiles;
+        xa.xs_bytes = xs_bytes;
+        xa.err = err;
         xa.rows = (mtiles - 1) * wide::kMmaMaxN + (((M - (mtiles - 1) * wide::kMmaMaxN) + 15) & ~15);
         const int64_t blocks = (xa.rows * nkb * 8 + 255) / 256;
         if (blocks > INT32_MAX) return LEAN_ERR_SHAPE;
@@ -338,6 +344,7 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
     a.step_vecs = g.step_vecs;
     a.group_vecs = g.group_vecs;
     a.err = err;
+    a.xs_bytes = xs ? xs_bytes : 0;
     a.mg = make_magic();
     if (xs) {
         // x -> bf16 hi / lo operand tiles, once
@@ -348,6 +355,8 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
         xa.K = (int)g.K;
         xa.nkb = nkb;
         xa.mtiles = (int)mtiles;
+        xa.xs_bytes = xs_bytes;
+        xa.err = err;
         xa.rows = (mtiles - 1) * kMmaMaxN + (((M - (mtiles - 1) * kMmaMaxN) + 15) & ~15);
         const int64_t blocks = (xa.rows * nkb * 8 + 255) / 256;
         if (blocks > INT32_MAX) return LEAN_ERR_SHAPE;
@@ -431,6 +440,10 @@ lean_status launch_gemv(const HostProb *ph, int n, int M, unsigned flags, bool o
     a.cl = cl;
     a.M = M;
     a.pad = 0;
+    a.err = nullptr;
+#ifdef LEAN_DEBUG
+    a.err = error_word();
+#endif
     a.mg = make_magic();
     int cta = 0;
     for (int i = 0; i < n; ++i) {
@@ -647,6 +660,8 @@ lean_status launch_stream(const HostProb *ph, int n, unsigned flags, void *ws, i
             xa.nprob = n;
             xa.int8 = (flags & LEAN_FLAG_X_INT8) ? 1 : 0;
             xa.xq = static_cast<uint8_t *>(ws) + wl.xq_off;
+            xa.xq_bytes = wl.cnt_off - wl.xq_off;
+            xa.err = err;
             for (int i = 0; i < n; ++i) {
                 xa.p[i].x = ph[i].x;
                 xa.p[i].xq0 = a.p[i].xq0;

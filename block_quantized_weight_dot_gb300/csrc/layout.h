@@ -40,6 +40,9 @@ constexpr int kXqBlockBytes = 160;
 
 enum Fmt { Q4_0 = 0, Q8_0 = 1, I8_B64 = 2, Q6_K = 3 };
 
+// Device error word bit of a LEAN_DEBUG build's index check (debug.cuh).
+constexpr unsigned kErrBounds = 32u;
+
 inline int block_elems(int fmt) {
     switch (fmt) {
     case Q4_0: return 32;

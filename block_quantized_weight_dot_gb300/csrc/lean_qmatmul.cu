@@ -32,9 +32,7 @@ __global__ void wait_selftest_kernel(unsigned *err, uint64_t limit_ns) {
 }
 }  // namespace
 
-namespace {
-
-bool aligned(const void *p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+namespace lean {
 
 // Device address of the error word on the current device (looked up once).
 unsigned *error_word() {
@@ -50,6 +48,12 @@ unsigned *error_word() {
     }
     return p;
 }
+
+}  // namespace lean
+
+namespace {
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
 template <int FMT>
 lean_status run_stream(const HostProb *ph, int n, unsigned flags, void *ws, int64_t wsb,
@@ -319,6 +323,21 @@ lean_status lean_wait_selftest(unsigned limit_us, void *stream) {
     cudaGetLastError();
     wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err, (uint64_t)limit_us * 1000u);
     return cudaGetLastError() == cudaSuccess ? LEAN_OK : LEAN_ERR_CUDA;
+}
+
+lean_status lean_device_status(int clear) {
+    const unsigned v = lean_device_error(clear);
+    if (v == 0xFFFFFFFFu) return LEAN_ERR_CUDA;
+    if (v & kErrBounds) return LEAN_ERR_KERNEL_BOUNDS;
+    return v ? LEAN_ERR_DEVICE : LEAN_OK;
+}
+
+int lean_debug_build(void) {
+#ifdef LEAN_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 unsigned lean_device_error(int clear) {

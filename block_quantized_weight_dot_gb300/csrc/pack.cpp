@@ -187,6 +187,8 @@ const char *lean_status_str(int status) {
     case LEAN_ERR_NULL: return "null pointer";
     case LEAN_ERR_ALIGN: return "misaligned pointer";
     case LEAN_ERR_CUDA: return "CUDA runtime error";
+    case LEAN_ERR_KERNEL_BOUNDS: return "a kernel met an index outside its buffers (LEAN_DEBUG build)";
+    case LEAN_ERR_DEVICE: return "a kernel reported an error in the device error word";
     }
     return "unknown status";
 }

@@ -24,6 +24,7 @@
 #include <cooperative_groups.h>
 #include <stdint.h>
 
+#include "debug.cuh"
 #include "decode.cuh"
 #include "layout.h"
 #include "ptx.cuh"
@@ -74,6 +75,7 @@ struct GemvArgs {
     int cl;  // CTAs per cluster (K split), the same for every problem
     int M;   // rows of x (<= MT of the kernel); x[M][K], y[M][N]
     int pad;
+    unsigned *err;  // device error word (LEAN_DEBUG index checks)
     Magic mg;
     GemvProb p[NP];
 };
@@ -82,16 +84,21 @@ struct GemvArgs {
 // GemvProb)
 template <int FMT>
 __device__ __forceinline__ void gemv_load(BlockFrag<FMT> &f, const GemvProb &p, const uint8_t *grp,
-                                          int c) {
+                                          int c, unsigned *err) {
     constexpr int VPB = BlockTraits<FMT>::VPB;
     const int s = c >> 3, i = c & 7;
     const int nblk = s == p.steps - 1 ? p.last_blocks : 8;
     const uint8_t *step = grp + (int64_t)s * p.step_vecs * kVecBytes;
+    const int64_t wbytes = (int64_t)((p.N + kRowsPerGroup - 1) / kRowsPerGroup) * p.group_vecs * kVecBytes;
 #pragma unroll
-    for (int j = 0; j < VPB; ++j)
-        f.v[j] = __ldg(reinterpret_cast<const uint4 *>(step + (i * VPB + j) * kVecBytes));
+    for (int j = 0; j < VPB; ++j) {
+        const uint8_t *vp = step + (i * VPB + j) * kVecBytes;
+        f.v[j] = LEAN_SPAN(vp - p.W, 16, wbytes, err) ? __ldg(reinterpret_cast<const uint4 *>(vp))
+                                                     : make_uint4(0u, 0u, 0u, 0u);
+    }
     const unsigned short *sv = reinterpret_cast<const unsigned short *>(step + nblk * VPB * kVecBytes);
-    f.d = h2f(__ldg(sv + i));
+    f.d = LEAN_SPAN(reinterpret_cast<const uint8_t *>(sv + i) - p.W, 2, wbytes, err) ? h2f(__ldg(sv + i))
+                                                                                    : 0.f;
 }
 
 // grid.x = sum over problems of groups * cl; cluster = (cl, 1, 1);
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
     BlockFrag<FMT> f[NB];
 #pragma unroll
     for (int i = 0; i < NB; ++i)
-        if (w0 + i < w1) gemv_load<FMT>(f[i], p, grp, w0 + i);
+        if (w0 + i < w1) gemv_load<FMT>(f[i], p, grp, w0 + i, a.err);
     const Magic mg = pin_fmt<FMT>(a.mg);
     pdl_wait();  // x may come from the previous kernel on the stream
 
@@ -146,7 +153,7 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
     for (int i = threadIdx.x; i < MT * nv; i += kGemvThreads) {
         const int m = i / nv, v = i % nv;
         float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (m < a.M)
+        if (m < a.M && LEAN_SPAN((int64_t)m * p.K + (int64_t)c0 * E + 4 * v, 4, (int64_t)a.M * p.K, a.err))
             val = reinterpret_cast<const float4 *>(p.x + (int64_t)m * p.K + (int64_t)c0 * E)[v];
         reinterpret_cast<float4 *>(xs + m * XS)[v] = val;
     }
@@ -171,7 +178,9 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
         red[i] = s;  // warp 0's slots: row m = i / 32, lane i % 32
         const int m = i >> 5;
         const int64_t n = g * kRowsPerGroup + (i & 31);
-        if (!SWIGLU && a.cl == 1 && m < a.M && n < p.N) p.y[(int64_t)m * p.N + n] = s;
+        if (!SWIGLU && a.cl == 1 && m < a.M && n < p.N &&
+            LEAN_IN((int64_t)m * p.N + n, (int64_t)a.M * p.N, a.err))
+            p.y[(int64_t)m * p.N + n] = s;
     }
     if (!SWIGLU && a.cl == 1) return;
     cg::cluster_group cluster = cg::this_cluster();
@@ -183,12 +192,13 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
             if (!SWIGLU) {
                 float s = red[i];
                 for (int r = 1; r < a.cl; ++r) s += cluster.map_shared_rank(red, r)[i];
-                if (m < a.M && n < p.N) p.y[(int64_t)m * p.N + n] = s;
+                if (m < a.M && n < p.N && LEAN_IN((int64_t)m * p.N + n, (int64_t)a.M * p.N, a.err))
+                    p.y[(int64_t)m * p.N + n] = s;
             } else {
                 float gs = red[i], us = 0.f;
                 for (int r = 1; r < ks; ++r) gs += cluster.map_shared_rank(red, r)[i];
                 for (int r = ks; r < a.cl; ++r) us += cluster.map_shared_rank(red, r)[i];
-                if (n < p.N) p.y[n] = gs / (1.f + expf(-gs)) * us;  // silu(g) * u
+                if (n < p.N && LEAN_IN(n, p.N, a.err)) p.y[n] = gs / (1.f + expf(-gs)) * us;  // silu(g) * u
             }
         }
     }

@@ -59,6 +59,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "debug.cuh"
 #include "decode.cuh"
 #include "layout.h"
 #include "ptx.cuh"
@@ -185,6 +186,7 @@ struct MmaArgs {
     int steps, last_blocks, step_vecs;
     int64_t groups;
     int64_t group_vecs;
+    int64_t xs_bytes;   // bytes of the split x (0 without)
     unsigned *err;
     Magic mg;
 };
@@ -195,6 +197,8 @@ struct XsplitArgs {
     int M, K, nkb;
     int mtiles;
     int64_t rows;  // padded rows over all tiles
+    int64_t xs_bytes;
+    unsigned *err;  // device error word (LEAN_DEBUG index checks)
 };
 
 // ---- tcgen05 wrappers ------------------------------------------------------------
@@ -348,7 +352,7 @@ static __global__ void __launch_bounds__(256) xsplit_kernel(const XsplitArgs a) 
     const int kb = p >> 3, k8 = p & 7;
     const int64_t k = (int64_t)kb * kMmaKB + 8 * k8;
     float v[8];
-    if (m < a.M && k < a.K) {
+    if (m < a.M && k < a.K && LEAN_SPAN(m * a.K + k, 8, (int64_t)a.M * a.K, a.err)) {
         const float *src = a.x + m * a.K + k;
         const float4 p0 = __ldg(reinterpret_cast<const float4 *>(src));
         const float4 p1 = __ldg(reinterpret_cast<const float4 *>(src + 4));
@@ -360,6 +364,7 @@ static __global__ void __launch_bounds__(256) xsplit_kernel(const XsplitArgs a) 
     }
     uint8_t *piece = a.xs + t * mma_xs_tile_bytes(a.nkb) + (int64_t)kb * 2 * mma_b_bytes(mpad);
     const uint32_t off = tile_off(mpad, mm, 8 * k8);
+    if (!LEAN_SPAN(piece + mma_b_bytes(mpad) + off - a.xs, 16, a.xs_bytes, a.err)) return;
     split_store8(v, piece + off, piece + mma_b_bytes(mpad) + off);
 }
 
@@ -387,6 +392,16 @@ __device__ __forceinline__ uint32_t raw_copy(const MmaArgs &a, int64_t gi, int64
     const int nblk = s == a.steps - 1 ? a.last_blocks : 8;
     const int nb = FMT == Q4_0 || FMT == Q8_0 ? nblk : FMT == I8_B64 ? min(4, nblk - i0) : 1;
     const uint32_t qbytes = (uint32_t)(nb * VPB * kVecBytes);
+    {
+        // both copies inside the packed matrix (else neither is made and the
+        // slot's barrier does not count their bytes)
+        const int64_t wbytes = a.groups * a.group_vecs * kVecBytes;
+        const int64_t sbase = (gi * a.group_vecs + s * a.step_vecs) * kVecBytes;
+        const bool in_q = LEAN_SPAN(sbase + (int64_t)i0 * VPB * kVecBytes, qbytes, wbytes, bar ? a.err : nullptr);
+        const bool in_s = LEAN_SPAN(sbase + (int64_t)nblk * VPB * kVecBytes, kVecBytes, wbytes,
+                                    bar ? a.err : nullptr);
+        if (!(in_q && in_s)) return 0u;
+    }
     if (bar) {
         const uint8_t *step = a.W + (gi * a.group_vecs + s * a.step_vecs) * kVecBytes;
         if ((FMT == Q4_0 || FMT == Q8_0) && nb == 8) {
@@ -611,10 +626,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
                 const int s = j & 3;
                 if (j >= BS && !mma_wait(&a_done[s], ((uint32_t)(j >> 2) & 1u) ^ 1u, abort_s)) break;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&b_full[s], (uint32_t)bbytes);
+                    const uint8_t *src = xs_tile + (int64_t)(kb0 + j) * bbytes;
+                    const bool in = LEAN_SPAN(src - a.xs, bbytes, a.xs_bytes, a.err);
+                    mbar_arrive_expect_tx(&b_full[s], in ? (uint32_t)bbytes : 0u);
                     if (j == 0) pdl_wait();  // the split x comes from the kernel before
-                    bulk_g2s(bring + s * bbytes, xs_tile + (int64_t)(kb0 + j) * bbytes,
-                             (uint32_t)bbytes, &b_full[s]);
+                    if (in) bulk_g2s(bring + s * bbytes, src, (uint32_t)bbytes, &b_full[s]);
                 }
                 __syncwarp();
                 issued = j + 1;
@@ -815,7 +831,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
                     const int i = ct + qq * kMmaConvThreads;
                     const int m = i % mpad;
                     const int64_t k = kb * kMmaKB + 8 * (i / mpad);
-                    if (i < mpad * 8 && m < mt && k < a.K) {
+                    if (i < mpad * 8 && m < mt && k < a.K &&
+                        LEAN_SPAN((int64_t)(m0 + m) * a.K + k, 8, (int64_t)a.M * a.K, a.err)) {
                         const float *src = a.x + (int64_t)(m0 + m) * a.K + k;
                         xv[qq][0] = __ldg(reinterpret_cast<const float4 *>(src));
                         xv[qq][1] = __ldg(reinterpret_cast<const float4 *>(src + 4));
@@ -861,7 +878,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
             float *yc = a.y + (int64_t)(m0 + c0) * a.N + nq;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-                if (c0 + i < mt) yc[(int64_t)i * a.N] = acc[i];
+                if (c0 + i < mt && LEAN_IN((int64_t)(m0 + c0 + i) * a.N + nq, (int64_t)a.M * a.N, a.err))
+                    yc[(int64_t)i * a.N] = acc[i];
         }
     } else {
         // partial y of this CTA into shared memory, P[m][row] (the rings are
@@ -903,11 +921,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
                     }
                 if (m < mt) {
                     float *yr = a.y + (int64_t)(m0 + m) * a.N;
-                    const int64_t nr = n0 + 4 * r4;
-                    if (nr < a.N) yr[nr] = s.x;
-                    if (nr + 1 < a.N) yr[nr + 1] = s.y;
-                    if (nr + 2 < a.N) yr[nr + 2] = s.z;
-                    if (nr + 3 < a.N) yr[nr + 3] = s.w;
+                    const int64_t nr = n0 + 4 * r4, yo = (int64_t)(m0 + m) * a.N + nr, ye = (int64_t)a.M * a.N;
+                    if (nr < a.N && LEAN_IN(yo, ye, a.err)) yr[nr] = s.x;
+                    if (nr + 1 < a.N && LEAN_IN(yo + 1, ye, a.err)) yr[nr + 1] = s.y;
+                    if (nr + 2 < a.N && LEAN_IN(yo + 2, ye, a.err)) yr[nr + 2] = s.z;
+                    if (nr + 3 < a.N && LEAN_IN(yo + 3, ye, a.err)) yr[nr + 3] = s.w;
                 }
             }
         }

@@ -13,6 +13,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "debug.cuh"
 #include "decode.cuh"
 #include "layout.h"
 #include "ptx.cuh"
@@ -34,6 +35,7 @@ struct SimtArgs {
     int rg;            // row groups per CTA
     int wpr;           // warps per row group inside a CTA
     int xs_stride;     // floats per x row in shared memory
+    unsigned *err;     // device error word (LEAN_DEBUG index checks)
     Magic mg;
 };
 
@@ -58,12 +60,17 @@ __device__ __forceinline__ void load_block(BlockFrag<FMT> &f, const SimtArgs &a,
     const int s = (int)(c >> 3), i = (int)(c & 7);
     const int nblk = s == a.steps - 1 ? a.last_blocks : 8;
     const uint8_t *step = grp + (int64_t)s * a.step_vecs * kVecBytes;
+    const int64_t wbytes = a.groups * a.group_vecs * kVecBytes;  // the packed matrix
 #pragma unroll
-    for (int j = 0; j < VPB; ++j)
-        f.v[j] = __ldg(reinterpret_cast<const uint4 *>(step + (i * VPB + j) * kVecBytes));
+    for (int j = 0; j < VPB; ++j) {
+        const uint8_t *vp = step + (i * VPB + j) * kVecBytes;
+        f.v[j] = LEAN_SPAN(vp - a.W, 16, wbytes, a.err) ? __ldg(reinterpret_cast<const uint4 *>(vp))
+                                                       : make_uint4(0u, 0u, 0u, 0u);
+    }
     const unsigned short *sv =
         reinterpret_cast<const unsigned short *>(step + nblk * VPB * kVecBytes);
-    f.d = h2f(__ldg(sv + i));
+    f.d = LEAN_SPAN(reinterpret_cast<const uint8_t *>(sv + i) - a.W, 2, wbytes, a.err) ? h2f(__ldg(sv + i))
+                                                                                       : 0.f;
 }
 
 // tot[m] += sum over the block of w * x[m]; xs = the block's x for row 0
@@ -179,7 +186,10 @@ __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
     for (int m = 0; m < MT && m < a.M; ++m) {
         const float4 *src = reinterpret_cast<const float4 *>(a.x + (int64_t)m * a.K + e0);
         float4 *dst = reinterpret_cast<float4 *>(xs + m * a.xs_stride);
-        for (int i = threadIdx.x; i < (elen >> 2); i += blockDim.x) dst[i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < (elen >> 2); i += blockDim.x)
+            dst[i] = LEAN_SPAN((int64_t)m * a.K + e0 + 4 * i, 4, (int64_t)a.M * a.K, a.err)
+                         ? __ldg(src + i)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
 
@@ -211,7 +221,8 @@ __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
             const int gq = i / (MT * 32), rest = i % (MT * 32);
             const int m = rest >> 5;
             const int64_t n = (g0 + gq) * kRowsPerGroup + (rest & 31);
-            if (m < a.M && n < a.N) a.y[(int64_t)m * a.N + n] = red[(gq * a.wpr * MT) * 32 + rest];
+            if (m < a.M && n < a.N && LEAN_IN((int64_t)m * a.N + n, (int64_t)a.M * a.N, a.err))
+                a.y[(int64_t)m * a.N + n] = red[(gq * a.wpr * MT) * 32 + rest];
         }
         return;
     }
@@ -225,7 +236,8 @@ __global__ void __launch_bounds__(512) qmm_simt_kernel(const SimtArgs a) {
             for (int r = 1; r < a.cl; ++r) s += cluster.map_shared_rank(red, r)[slot];
             const int m = rest >> 5;
             const int64_t n = (g0 + gq) * kRowsPerGroup + (rest & 31);
-            if (m < a.M && n < a.N) a.y[(int64_t)m * a.N + n] = s;
+            if (m < a.M && n < a.N && LEAN_IN((int64_t)m * a.N + n, (int64_t)a.M * a.N, a.err))
+                a.y[(int64_t)m * a.N + n] = s;
         }
     }
     cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
@@ -290,7 +302,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const SimtArgs a, float *w
     BlockFrag<FMT> f;
     load_block<FMT>(f, a, a.W + g * a.group_vecs * kVecBytes + lane * kVec, c);
     const int64_t n = g * kRowsPerGroup + lane;
-    if (n >= a.N) return;
+    if (n >= a.N || !LEAN_SPAN(n * a.K + c * E, E, (int64_t)a.N * a.K, a.err)) return;
     store_block<FMT>(f, a.mg, w + n * a.K + c * E);
 }
 
@@ -310,6 +322,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const SimtArgs a, const int3
     const int64_t i = item / a.blocks, c = item % a.blocks;
     const int64_t n = ids[i];
     float *o = out + i * a.K + c * E;
+    if (!LEAN_SPAN(i * a.K + c * E, E, n_ids * a.K, a.err)) return;
     if (n < 0 || n >= a.N) {
         const float4 nan4 = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
                                         __int_as_float(0x7fc00000), __int_as_float(0x7fc00000));

@@ -61,6 +61,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "debug.cuh"
 #include "decode.cuh"
 #include "layout.h"
 #include "ptx.cuh"
@@ -395,6 +396,8 @@ struct XprepArgs {
     int nprob;
     int int8;  // 1: quantize x to int8 (LEAN_FLAG_X_INT8) instead of the exact planes
     uint8_t *xq;
+    int64_t xq_bytes;  // bytes of the plane region
+    unsigned *err;     // device error word (LEAN_DEBUG index checks)
     XprepProb p[NP];
 };
 template <int FMT, int NP>
@@ -415,7 +418,7 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ Xpre
     if (a.int8) {
 #pragma unroll
         for (int u = 0; u < kXprepBlocks; ++u)
-            if (b0 + u < p.nb)
+            if (b0 + u < p.nb && LEAN_SPAN(p.xq0 + (int64_t)(b0 + u) * kXqBytes, kXqBytes, a.xq_bytes, a.err))
                 x_block_store_int8<FMT>(v[u], a.xq + p.xq0 + (int64_t)(b0 + u) * kXqBytes, lane);
         return;
     }
@@ -433,7 +436,8 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ Xpre
         int mode = 0;
 #pragma unroll
         for (int j = 0; j < G; ++j) mode = max(mode, tiers[c0 + j]);
-        x_block_store<FMT>(xb[u], mode, a.xq + p.xq0 + (int64_t)(b0 + u) * kXqBytes, lane);
+        if (LEAN_SPAN(p.xq0 + (int64_t)(b0 + u) * kXqBytes, kXqBytes, a.xq_bytes, a.err))
+            x_block_store<FMT>(xb[u], mode, a.xq + p.xq0 + (int64_t)(b0 + u) * kXqBytes, lane);
     }
 }
 
@@ -875,13 +879,23 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
             if (planes) {
                 xb = q.nbc * (C::E / 32) * kXqBytes;
                 xs = a.xq + p.xq0 + (e0 / 32) * kXqBytes;
+                if (!LEAN_SPAN((e0 / 32) * kXqBytes, xb, (int64_t)(p.K / 32) * kXqBytes, a.err)) xb = 0;
             } else {
                 xb = q.nbc * C::E * 4;
                 xs = reinterpret_cast<const uint8_t *>(p.x + e0);
+                if (!LEAN_SPAN(e0 * 4, xb, (int64_t)p.K * 4, a.err)) xb = 0;
             }
-            mbar_arrive_expect_tx(&full[sl], ng * (qbytes + kVecBytes) + xb);
             const bool merged = q.sub * C::BPC + q.nbc == q.nblk;  // chunk ends at the scale vector
+            // (LEAN_DEBUG) only copies inside the packed matrix are made and counted
+            const int64_t wbytes = p.groups * p.group_vecs * kVecBytes;
+            bool w_in = true;
             for (int w = 0; w < ng; ++w) {
+                const int64_t so = ((gb * L::GPU + w) * p.group_vecs + (int64_t)q.s * SV) * kVecBytes;
+                w_in = w_in && LEAN_SPAN(so + q.sub * C::BPC * C::VPB * kVecBytes, qbytes, wbytes, a.err) &&
+                       LEAN_SPAN(so + q.nblk * C::VPB * kVecBytes, kVecBytes, wbytes, a.err);
+            }
+            mbar_arrive_expect_tx(&full[sl], (w_in ? ng * (qbytes + kVecBytes) : 0u) + xb);
+            for (int w = 0; w < ng && w_in; ++w) {
                 const uint8_t *step =
                     p.W + ((gb * L::GPU + w) * p.group_vecs + (int64_t)q.s * SV) * kVecBytes;
                 uint8_t *dst = base + w * L::CHUNK_BYTES;
@@ -896,7 +910,7 @@ __global__ void __launch_bounds__(kStreamThreads, (StreamRing<FMT, PL>::CPS))
             advance();
         };
         auto issue_x = [&](int sl, const uint8_t *xs, uint32_t xb) {
-            bulk_g2s(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES, xs, xb, &full[sl]);
+            if (xb) bulk_g2s(ring + sl * L::SLOT_BYTES + L::GPU * L::CHUNK_BYTES, xs, xb, &full[sl]);
         };
         // after a timeout: let the copies already issued (units j - S .. j - 1)
         // land before the CTA can exit

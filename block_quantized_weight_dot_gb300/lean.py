@@ -16,9 +16,13 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "liblean_qmatmul.so")
+# the LEAN_DEBUG build of the same ABI (build.build(debug=True)): every kernel
+# checks its global-memory indices; for test runs (open_library / use_library)
+DEBUG_LIB_PATH = os.path.join(_HERE, "liblean_qmatmul_debug.so")
 
 LEAN_Q4_0, LEAN_Q8_0, LEAN_I8_B64, LEAN_Q6_K = 0, 1, 2, 3
-LEAN_OK, LEAN_ERR_FORMAT, LEAN_ERR_SHAPE, LEAN_ERR_NULL, LEAN_ERR_ALIGN, LEAN_ERR_CUDA = range(6)
+(LEAN_OK, LEAN_ERR_FORMAT, LEAN_ERR_SHAPE, LEAN_ERR_NULL, LEAN_ERR_ALIGN, LEAN_ERR_CUDA,
+ LEAN_ERR_KERNEL_BOUNDS, LEAN_ERR_DEVICE) = range(8)
 LEAN_FLAG_EARLY_WEIGHTS = 1
 LEAN_FLAG_X_PLANES = 2
 LEAN_FLAG_STREAM = 4
@@ -45,6 +49,8 @@ SIGNATURES = {
     "lean_batch_workspace_bytes": (_i64, [_int, _int, _vp]),
     "lean_qmatmul_batch": (_int, [_int, _int, _vp, ctypes.c_uint, _vp, _i64, _vp]),
     "lean_device_error": (ctypes.c_uint, [_int]),
+    "lean_device_status": (_int, [_int]),
+    "lean_debug_build": (_int, []),
     "lean_wait_selftest": (_int, [ctypes.c_uint, _vp]),
     "lean_quantize": (_int, [_int, _vp, _vp, _i64, _i64, _int]),
     "lean_qmatmul_fixed_ws": (_int, [_int, _vp, _vp, _vp, _i64, _i64, ctypes.c_uint, _vp]),
@@ -66,11 +72,10 @@ class LeanError(RuntimeError):
         super().__init__("%s failed: %s (status %d)" % (fn, status_str(status), status))
 
 
-def _load():
-    if not os.path.exists(LIB_PATH):
-        raise ImportError("liblean_qmatmul.so is not built: run "
-                          "`python -c \"import __graft_entry__ as g; g.build()\"`")
-    lib = ctypes.CDLL(LIB_PATH)
+def open_library(path: str):
+    """A ctypes handle on a build of this ABI (the product library or its
+    LEAN_DEBUG build), with every declared signature set."""
+    lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype = res
@@ -78,7 +83,22 @@ def _load():
     return lib
 
 
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("liblean_qmatmul.so is not built: run "
+                          "`python -c \"import __graft_entry__ as g; g.build()\"`")
+    return open_library(LIB_PATH)
+
+
 _lib = _load()
+
+
+def use_library(lib):
+    """Route every call of this module through `lib` (a handle from
+    open_library); returns the handle used until now."""
+    global _lib
+    prev, _lib = _lib, lib
+    return prev
 
 
 def _addr(buf):
@@ -263,6 +283,16 @@ def lean_quantize(fmt: int, w, N: int, K: int, threads: int = 0):
     _check("lean_quantize", _lib.lean_quantize(fmt, w.ctypes.data, out.ctypes.data, N, K,
                                                 threads))
     return out[:nbytes]
+
+
+def lean_device_status(clear: bool = True) -> int:
+    """The device error word as a status (LEAN_OK, LEAN_ERR_KERNEL_BOUNDS,
+    LEAN_ERR_DEVICE or LEAN_ERR_CUDA); returned, not raised."""
+    return _lib.lean_device_status(1 if clear else 0)
+
+
+def lean_debug_build() -> int:
+    return _lib.lean_debug_build()
 
 
 def lean_wait_selftest(limit_us: int, stream=None) -> None:

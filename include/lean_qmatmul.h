@@ -86,24 +86,39 @@ typedef enum {
                             or a size beyond the library's limits           */
     LEAN_ERR_NULL = 3,   /* a required pointer is NULL                      */
     LEAN_ERR_ALIGN = 4,  /* a pointer is not aligned as documented          */
-    LEAN_ERR_CUDA = 5    /* the CUDA runtime reported an error              */
+    LEAN_ERR_CUDA = 5,   /* the CUDA runtime reported an error              */
+    LEAN_ERR_KERNEL_BOUNDS = 6, /* (lean_device_status) a kernel of a LEAN_DEBUG
+                            build met an index outside its buffers          */
+    LEAN_ERR_DEVICE = 7  /* (lean_device_status) a kernel reported another
+                            error in the device error word                  */
 } lean_status;
 
-/* Weights per block: 32, 32, 64, 256.  0 for an unknown fmt. */
+/* Weights per block: 32, 32, 64, 256.  0 for an unknown fmt.
+ * Pages: "oxinfer" crate page, How it works (quant.rs: Q8 and Q4_0 blocks of
+ * 32); "wgpu-llm" README, INT8 mode (block size 64); "lean" README, model
+ * table (Q6_K). */
 int lean_block_elems(int fmt);
 
-/* Canonical bytes per block: 18, 34, 66, 210.  0 for an unknown fmt. */
+/* Canonical bytes per block: 18, 34, 66, 210.  0 for an unknown fmt.
+ * Pages: as lean_block_elems (fp16 scales: "oxinfer" crate page, How it
+ * works, Q4_0 "f16 scale"; the other sizes are the same reading). */
 int64_t lean_block_bytes(int fmt);
 
-/* Canonical bytes of an N x K matrix, or -1 on a bad fmt or shape. */
+/* Canonical bytes of an N x K matrix, or -1 on a bad fmt or shape.
+ * Pages: "oxinfer" crate page, Pre-quantized checkpoints (a quantized matrix
+ * is its quant bytes plus its scales). */
 int64_t lean_canonical_bytes(int fmt, int64_t N, int64_t K);
 
 /* Packed (device layout) bytes of an N x K matrix, or -1 on a bad fmt or
  * shape.  Rows are padded up to a multiple of 32 and the scale plane to whole
- * 16-byte vectors, so this is a little more than lean_canonical_bytes(). */
+ * 16-byte vectors, so this is a little more than lean_canonical_bytes().
+ * Pages: "oxinfer" crate page, Pre-quantized checkpoints (weights kept "in
+ * exactly the in-memory layout of the kernels"). */
 int64_t lean_packed_bytes(int fmt, int64_t N, int64_t K);
 
-/* Host-side repacking, canonical -> packed.  canon_host holds
+/* Host-side repacking, canonical -> packed (pages: as lean_packed_bytes;
+ * here done once at upload, as the pages' loader borrows the file's blocks
+ * without copying).  canon_host holds
  * lean_canonical_bytes(fmt,N,K) bytes; packed_host receives
  * lean_packed_bytes(fmt,N,K) bytes (padding is written as zeros).  Both are
  * host pointers with no alignment requirement.  Blocks are moved bit for bit:
@@ -111,11 +126,15 @@ int64_t lean_packed_bytes(int fmt, int64_t N, int64_t K);
 lean_status lean_pack(int fmt, const void *canon_host, void *packed_host,
                       int64_t N, int64_t K);
 
-/* Host-side inverse of lean_pack: packed -> canonical, byte for byte. */
+/* Host-side inverse of lean_pack: packed -> canonical, byte for byte (no
+ * counterpart on the pages: the round trip is this library's check of its
+ * own layout). */
 lean_status lean_unpack_canonical(int fmt, const void *packed_host, void *canon_host,
                                   int64_t N, int64_t K);
 
-/* Device dequantisation: w_dev[n*K + k] = w[n][k] as fp32 (exact: every
+/* Device dequantisation ("oxinfer" crate page, Performance: quantized
+ * prefill dequantizes to f32; Platforms and accelerators: weights dequantized
+ * to f32 in threadgroup memory): w_dev[n*K + k] = w[n][k] as fp32 (exact: every
  * weight of these formats is an fp32 value).  W_packed_dev: 16-byte aligned
  * device pointer to lean_packed_bytes() bytes made by lean_pack.  w_dev:
  * 16-byte aligned device buffer of N*K floats, overwritten. */
@@ -141,6 +160,9 @@ lean_status lean_embed_rows(int fmt, const void *W_packed_dev, const int32_t *id
                             float *out_dev, int64_t n_ids, int64_t N, int64_t K, void *stream);
 
 /* The product.  y[m][n] = sum_k w[n][k] * x[m][k], accumulated in fp32.
+ * Pages: "oxinfer" crate page, Performance (decode streams every weight once
+ * per token) and How it works (decode tiles over quantized rows); "wgpu-llm"
+ * README, Architecture at a Glance (every layer's linears).
  *   W_packed_dev  device, 16-byte aligned, lean_packed_bytes(fmt,N,K) bytes
  *                 made by lean_pack (read only)
  *   x_dev         device, 16-byte aligned, x[M][K] fp32 row-major (read only)
@@ -148,14 +170,15 @@ lean_status lean_embed_rows(int fmt, const void *W_packed_dev, const int32_t *id
  *   stream        cudaStream_t as void*
  * M = 1 is the decode GEMV: a product whose row groups fit the GPU in one
  * wave runs on a kernel that loads all of its weights first and reduces on
- * chip, a larger one streams its weights through a TMA ring; M = 2..15 runs on
- * the CUDA cores with each
- * decoded weight reused M times; M >= 16 (lean_tensor_core_min_m()) runs on
- * the tcgen05 tensor cores
- * with split-bf16 operands (w = w_hi + w_lo, x = x_hi + x_lo, three MMAs into
- * fp32 accumulators), every format.  Accuracy: |y - y_exact| <= 1e-4 *
- * sum_k |w x| + 1e-6 per element.  Nothing is allocated: without a workspace
- * (lean_qmatmul_ws) the tensor-core path splits x inside each CTA. */
+ * chip, a larger one streams its weights through a TMA ring.  M = 2..15 runs
+ * on the CUDA cores with each decoded weight reused M times (when a row fits
+ * one wave; else a row-tiled kernel).  M >= 16 (lean_tensor_core_min_m())
+ * runs on the tcgen05 tensor cores, every format: up to 64 rows of x, the
+ * integer codes times x = x_hi + x_lo (bf16) with each block scale applied
+ * after the MMAs in fp32; more rows, w = w_hi + w_lo times x_hi + x_lo (three
+ * MMAs per K step).  Accuracy: |y - y_exact| <= 1e-4 * sum_k |w x| + 1e-6
+ * per element.  Nothing is allocated: without a workspace (lean_qmatmul_ws)
+ * the tensor-core path splits x inside each CTA. */
 lean_status lean_qmatmul(int fmt, const void *W_packed_dev, const float *x_dev,
                          float *y_dev, int64_t N, int64_t K, int64_t M, void *stream);
 
@@ -194,7 +217,9 @@ enum {
 };
 
 /* lean_qmatmul with launch flags (LEAN_FLAG_*; unknown bits are rejected
- * with LEAN_ERR_FORMAT).  flags = 0 is exactly lean_qmatmul. */
+ * with LEAN_ERR_FORMAT).  flags = 0 is exactly lean_qmatmul.  Pages: as
+ * lean_qmatmul; the flags serve the decode step's chain of small products
+ * ("oxinfer" crate page, How it works: ~200 small parallel regions a step). */
 lean_status lean_qmatmul_ex(int fmt, const void *W_packed_dev, const float *x_dev,
                             float *y_dev, int64_t N, int64_t K, int64_t M,
                             unsigned flags, void *stream);
@@ -220,17 +245,20 @@ lean_status lean_qmatmul_swiglu(int fmt, const void *W_gate_dev, const void *W_u
                                 const float *x_dev, float *h_dev, int64_t N, int64_t K,
                                 unsigned flags, void *stream);
 
-/* Rows of x from which lean_qmatmul uses the tensor cores (16). */
+/* Rows of x from which lean_qmatmul uses the tensor cores (16).  Pages:
+ * "oxinfer" crate page, Platforms and accelerators (the GPU takes matmuls of
+ * t >= 16 tokens). */
 int lean_tensor_core_min_m(void);
 
 /* Bytes of device workspace that lean_qmatmul_ws uses for this shape (0 when
  * it uses none: M = 2..15), or -1 on a bad fmt or shape.  M = 1: stream-K
  * partial sums and counters.  M >= 16: x split into bf16 hi / lo operand
- * tiles, 4 bytes per element of x with M padded to 16 per 256-row tile and K
- * to 64. */
+ * tiles, 4 bytes per element of x with M padded to 16 and K to 64.  (No
+ * counterpart on the pages: scratch of this library's kernels.) */
 int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);
 
-/* lean_qmatmul_ex with a caller-owned device workspace.  With a workspace the
+/* lean_qmatmul_ex with a caller-owned device workspace (pages: as
+ * lean_qmatmul; the workspace is this library's).  With a workspace the
  * M = 1 product splits K-steps evenly over all SMs, also inside a 32-row
  * group, and the CTA that finishes a split group last adds the parts up (in
  * a fixed order, so results stay deterministic); without one (NULL) every
@@ -283,10 +311,14 @@ typedef struct {
     int64_t N, K;
 } lean_problem;
 
-/* Workspace bytes for lean_qmatmul_batch over these problems, or -1. */
+/* Workspace bytes for lean_qmatmul_batch over these problems, or -1 (no
+ * counterpart on the pages). */
 int64_t lean_batch_workspace_bytes(int fmt, int count, const lean_problem *problems);
 
-/* problems: host array of `count` (1..LEAN_MAX_BATCH) descriptors, read during
+/* Pages: "wgpu-llm" README, Architecture at a Glance (N x (Attn + FFN): the
+ * independent linears of a layer); "oxinfer" crate page, How it works (a
+ * decode step issues ~200 small parallel regions, so dispatch cost matters).
+ * problems: host array of `count` (1..LEAN_MAX_BATCH) descriptors, read during
  * the call only.  workspace / workspace_bytes / flags as for lean_qmatmul_ws
  * (workspace may be NULL).  Outputs of different problems must not overlap
  * each other or any input.  On the x-plane path (Q4_0 / Q8_0 / I8_B64 with a
@@ -321,27 +353,45 @@ lean_status lean_qmatmul_fixed_ws(int fmt, const void *W_packed_dev, const float
                                   float *y_dev, int64_t N, int64_t K, unsigned flags,
                                   void *stream);
 
-/* Size in bytes of the fixed array behind lean_qmatmul_fixed_ws. */
+/* Size in bytes of the fixed array behind lean_qmatmul_fixed_ws (no
+ * counterpart on the pages). */
 int64_t lean_fixed_workspace_bytes(void);
 
-/* The device error word of the current device: non-zero when a kernel gave up
+/* No counterpart on the pages (their kernels run on the CPU, and their GPU
+ * backends report through the host API): the library's own fault reporting.
+ * The device error word of the current device: non-zero when a kernel gave up
  * waiting on one of its own pipeline barriers (a bounded wait timed out and
  * the kernel returned early; its outputs are then invalid) or met an index
  * out of its range.  Bits: 1 a stream consumer waited too long for a slot, 2
  * a stream producer for a free slot, 4 the tensor-core product for a stage, 8
- * lean_wait_selftest, 16 lean_embed_rows was given an id outside 0 .. N-1.  Reads it
+ * lean_wait_selftest, 16 lean_embed_rows was given an id outside 0 .. N-1, 32
+ * (LEAN_DEBUG builds only) a kernel computed an index outside the buffers its
+ * arguments describe and skipped that access.  Reads it
  * synchronously (the device is synchronised first) and clears it when
  * `clear` is non-zero.  Returns 0xFFFFFFFF if the word cannot be read. */
 unsigned lean_device_error(int clear);
 
-/* Self-test of the bounded waits: launches one 32-thread block on `stream`
+/* The device error word as a status, read and cleared as lean_device_error
+ * (clear non-zero): LEAN_OK when it is zero, LEAN_ERR_KERNEL_BOUNDS when bit
+ * 32 is set, LEAN_ERR_DEVICE for any other bit, LEAN_ERR_CUDA when the word
+ * cannot be read.  No counterpart on the pages. */
+lean_status lean_device_status(int clear);
+
+/* 1 when this library was built with LEAN_DEBUG (every kernel checks its
+ * global-memory indices against the buffers its arguments describe, skips an
+ * access outside them and sets bit 32 of the device error word; never a
+ * trap), else 0.  No counterpart on the pages. */
+int lean_debug_build(void);
+
+/* Self-test of the bounded waits (no counterpart on the pages): launches one
+ * 32-thread block on `stream`
  * that waits, with the same bounded mbarrier wait the kernels use, on a
  * barrier that nothing completes, gives up after `limit_us` microseconds
  * (1 .. 1000000) and sets bit 8 of the device error word.  The context stays
  * usable.  LEAN_ERR_SHAPE for a limit out of range. */
 lean_status lean_wait_selftest(unsigned limit_us, void *stream);
 
-/* Static description of a status code. */
+/* Static description of a status code (no counterpart on the pages). */
 const char *lean_status_str(int status);
 
 #ifdef __cplusplus

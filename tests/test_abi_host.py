@@ -122,3 +122,31 @@ def test_host_argument_errors(lean):
     assert f(0, buf.ctypes.data, buf.ctypes.data, 1, 33) == lean.LEAN_ERR_SHAPE
     for s in range(6):
         assert lean.status_str(s)
+
+
+def test_device_status_codes_and_build_kind(lean):
+    """LEAN_ERR_KERNEL_BOUNDS and LEAN_ERR_DEVICE are declared, described,
+    and the product library is the release build (no index checks)."""
+    import re
+    hdr = open(os.path.join(ROOT, "include", "lean_qmatmul.h")).read()
+    assert re.search(r"LEAN_ERR_KERNEL_BOUNDS\s*=\s*6", hdr)
+    assert re.search(r"LEAN_ERR_DEVICE\s*=\s*7", hdr)
+    assert lean.LEAN_ERR_KERNEL_BOUNDS == 6 and lean.LEAN_ERR_DEVICE == 7
+    assert "LEAN_DEBUG" in lean.status_str(lean.LEAN_ERR_KERNEL_BOUNDS)
+    assert "error word" in lean.status_str(lean.LEAN_ERR_DEVICE)
+    assert lean.lean_debug_build() == 0
+
+
+def test_library_keeps_its_own_statics(lean):
+    """The library binds its own symbols and has no GNU-unique ones, so two
+    builds loaded into one process (the release and the LEAN_DEBUG library)
+    keep separate per-device caches."""
+    import shutil
+    import subprocess
+    if not shutil.which("readelf"):
+        pytest.skip("readelf not installed")
+    lib = lib_build.LIB
+    syms = subprocess.run(["readelf", "--dyn-syms", "-W", lib], capture_output=True, text=True).stdout
+    assert "UNIQUE" not in syms
+    dyn = subprocess.run(["readelf", "-d", lib], capture_output=True, text=True).stdout
+    assert "SYMBOLIC" in dyn
