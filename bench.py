@@ -606,7 +606,7 @@ def main():
 def linear_path(lin, tc_min):
     if lin.M == 1:
         return "m1"  # one-wave kernel when the rows fit the GPU at once, else streaming
-    return "simt" if lin.M < tc_min else "mma"
+    return "cuda_cores" if lin.M < tc_min else "mma"
 
 
 def mma_issued_flops(lin):
