@@ -202,15 +202,55 @@ lean_status embed_fmt(const Geom &g, const uint8_t *W, const int32_t *ids, int64
 
 // --------------------------------------------------------- tensor-core path ---
 
-// K split of the tensor-core product: the cluster size that minimises
-// waves x (256-wide K slots per CTA + a fixed cost of about one slot for
-// set-up and epilogue), never more CTAs than slots.
-inline int mma_split(int64_t tiles, int nsl, int64_t slots) {
+
+// Clusters of c CTAs of `kern` (one CTA per SM) that fit the GPU at once:
+// cudaOccupancyMaxActiveClusters, which knows how the SMs are grouped (16
+// row tiles in clusters of 8 did not all fit in one wave).  Read once per
+// device and c; 0 when the query fails.
+template <typename Kern>
+inline int mma_active_clusters(Kern kern, int c, size_t smem, int threads) {
+    static std::atomic<int> cache[kMaxDevices][kMmaMaxSplit + 1];
+    const int dev = current_device();
+    if (dev < 0 || c < 1 || c > kMmaMaxSplit) return 0;
+    int v = cache[dev][c].load(std::memory_order_relaxed);
+    if (v == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)c, 1, 1);
+        cfg.blockDim = dim3((unsigned)threads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess || v <= 0) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        cache[dev][c].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// K split of a tensor-core product: the cluster size c that minimises
+// waves x (256-wide K slots per CTA + fixed + reduce when c > 1), in units of
+// one slot's time, the waves counted from the clusters that fit at once.
+// Constants from timing the Qwen2.5-3B FFN shapes (11008 x 2048 and 2048 x
+// 11008) at every c: for the integer-code kernel (M = 16, 64) a CTA's fixed
+// cost (start, epilogue) is about two slots and the cluster reduction 0.7;
+// the split-weight kernel's slots cost about three times as much, so its
+// fixed costs are smaller in slots (1 and 0.3).
+template <typename ClusterFn>
+inline int mma_split_clusters(int64_t tiles, int nsl, double fixed, double reduce, ClusterFn clusters) {
     int ks = 1;
     double best = 1e300;
     for (int c = 1; c <= kMmaMaxSplit && c <= nsl; ++c) {
-        const int64_t waves = (tiles * c + slots - 1) / slots;
-        const double cost = (double)waves * ((nsl + c - 1) / c + 1.0);
+        const int n = clusters(c);
+        if (n <= 0) continue;
+        const int64_t waves = (tiles + n - 1) / n;
+        const double cost = (double)waves * ((nsl + c - 1) / c + fixed + (c > 1 ? reduce : 0.0));
         if (cost < best - 1e-9) {
             best = cost;
             ks = c;
@@ -235,8 +275,7 @@ lean_status mma_wide_fmt(const Geom &g, const uint8_t *W, const float *x, float 
     const size_t smem = (size_t)wide::mma_smem_bytes<FMT>(mpad, RS);
     // one CTA per SM: the rings take most of the shared memory and all 512
     // tensor-memory columns are allocated
-    const int ks = mma_split(tiles * mtiles, nsl, (int64_t)sm_count());
-    if (tiles * ks > INT32_MAX || RS < 1) return LEAN_ERR_SHAPE;
+    if (RS < 1) return LEAN_ERR_SHAPE;
     const int64_t xs_bytes = wide::mma_xs_bytes(M, g.K);
     if (ws && ws_bytes < xs_bytes) return LEAN_ERR_SHAPE;
     uint8_t *xs = static_cast<uint8_t *>(ws);
@@ -248,7 +287,6 @@ lean_status mma_wide_fmt(const Geom &g, const uint8_t *W, const float *x, float 
     a.N = (int)g.N;
     a.K = (int)g.K;
     a.M = (int)M;
-    a.ks = ks;
     a.nkb = nkb;
     a.nsl = nsl;
     a.RS = RS;
@@ -287,6 +325,11 @@ lean_status mma_wide_fmt(const Geom &g, const uint8_t *W, const float *x, float 
     auto kern = xs ? wide::qmm_mma_kernel<FMT, true> : wide::qmm_mma_kernel<FMT, false>;
     std::atomic<uint64_t> &sd = xs ? smem_done : smem_done_x;
     if (!ensure_smem(kern, (size_t)wide::kMmaSmemLimit, sd)) return LEAN_ERR_CUDA;
+    const int ks = mma_split_clusters(tiles * mtiles, nsl, 1.0, 0.3, [&](int c) {
+        return mma_active_clusters(kern, c, smem, wide::kMmaThreads);
+    });
+    if (tiles * ks > INT32_MAX) return LEAN_ERR_SHAPE;
+    a.ks = ks;
     for (int64_t t0 = 0; t0 < mtiles; t0 += 65535) {
         a.m_base = (int)(t0 * wide::kMmaMaxN);
         cudaLaunchConfig_t cfg = {};
@@ -318,10 +361,7 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
     const int mpad = ((int)std::min<int64_t>(M, kMmaMaxN) + 15) & ~15;
     const int RS = mma_raw_slots<FMT>(mpad);
     const size_t smem = (size_t)mma_smem_bytes<FMT>(mpad, RS);
-    // one CTA per SM: the rings take most of the shared memory and all 512
-    // tensor-memory columns are allocated
-    const int ks = mma_split(tiles * mtiles, nsl, (int64_t)sm_count());
-    if (tiles * ks > INT32_MAX || RS < 1) return LEAN_ERR_SHAPE;
+    if (RS < 1) return LEAN_ERR_SHAPE;
     const int64_t xs_bytes = mma_xs_bytes(M, g.K);
     if (ws && ws_bytes < xs_bytes) return LEAN_ERR_SHAPE;
     uint8_t *xs = static_cast<uint8_t *>(ws);
@@ -333,7 +373,6 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
     a.N = (int)g.N;
     a.K = (int)g.K;
     a.M = (int)M;
-    a.ks = ks;
     a.nkb = nkb;
     a.nsl = nsl;
     a.RS = RS;
@@ -371,6 +410,13 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
     auto kern = xs ? qmm_mma_kernel<FMT, true> : qmm_mma_kernel<FMT, false>;
     std::atomic<uint64_t> &sd = xs ? smem_done : smem_done_x;
     if (!ensure_smem(kern, (size_t)kMmaSmemLimit, sd)) return LEAN_ERR_CUDA;
+    // one CTA per SM: the rings take most of the shared memory and all 512
+    // tensor-memory columns are allocated
+    const int ks = mma_split_clusters(tiles * mtiles, nsl, 2.0, 0.7, [&](int c) {
+        return mma_active_clusters(kern, c, smem, kMmaThreads);
+    });
+    if (tiles * ks > INT32_MAX) return LEAN_ERR_SHAPE;
+    a.ks = ks;
     for (int64_t t0 = 0; t0 < mtiles; t0 += 65535) {
         a.m_base = (int)(t0 * kMmaMaxN);
         cudaLaunchConfig_t cfg = {};
