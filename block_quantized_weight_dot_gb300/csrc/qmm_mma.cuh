@@ -26,34 +26,40 @@
 // warps split each CTA's x themselves.  qmm_mma_kernel computes one tile of
 // 128 weight rows against up to 64 rows of x: tcgen05.mma of shape M = 128
 // (weight rows) x N = mpad (rows of x padded to 16) x K = 16, A (the codes)
-// and D in tensor memory, B (the split x) in shared memory.  Roles:
-//   warp 16 (one lane)    streams the packed weights with one TMA bulk copy
+// and D in tensor memory, B (the split x) in shared memory.  Warp roles,
+// oldest first (the scheduler favours older warps, and the single-lane roles
+// pace the pipeline):
+//   warps 0-3             MMA issuers (NI of them): each takes every NI-th
+//                         scale group, into buffers of its own, and commits the
+//                         group to its D buffer (d_full) and its stage to
+//                         a_done, which frees the A stage and the B slot of the
+//                         same index.  The whole warp runs the loop on
+//                         warp-uniform values and one elected lane issues
+//                         (about 94 cycles per MMA and issuing warp, whatever N).
+//   warp 4 (one lane)     streams the packed weights with one TMA bulk copy
 //                         per 32-row group and 256-wide K slot into a ring of
 //                         raw slots (raw_full / raw_empty);
-//   warp 17 (one lane)    with split x, copies each 64-wide K block of it into
-//                         a ring of B stages (b_full);
-//   warps 0-7             per 64-wide K block ("stage"), turn the codes into
-//                         bf16 (thread t: row t % 128, half t / 128 of the
-//                         stage) and store them to a tensor-memory A stage
-//                         with tcgen05.st (a_full); without split x they also
-//                         fill B;
-//   warps 18-19 (lane 0)  issue the MMAs of alternate scale groups, each group
-//                         into one of four D buffers (d_full), and commit each
-//                         stage to a_done, which frees the A stage and the
-//                         stage's B slot (the B ring is no deeper than the A
-//                         ring, so a B slot's last user is found on the A
-//                         ring);
-//   warps 8-15            per scale group, read D_g (tcgen05.ld; warps 8-11
-//                         columns 0-31, warps 12-15 columns 32-63), free the
-//                         buffer (d_empty) and add d * D_g into fp32
-//                         registers with paired FMAs; the scale comes from the
-//                         raw slot, which these warps release too.
-// When the row tiles alone do not fill the GPU, a thread-block cluster of ks
-// CTAs splits K on slot boundaries; each CTA leaves its partial y in shared
-// memory and, after a cluster barrier, CTA r sums columns r*mpad/ks ..
+//   warp 5 (one lane)     with split x, copies each 64-wide K block of it into
+//                         a ring of B slots (b_full);
+//   warps 6-13            per scale group, read D_g (tcgen05.ld; 32 columns a
+//                         warp, two warps per lane quarter), free the buffer
+//                         (d_empty) and add d * D_g into fp32 registers; the
+//                         scale comes from the raw slot, which these warps
+//                         release too;
+//   warps 14-17           per two 64-wide K blocks ("stages"), turn the codes
+//                         of one row each into bf16 and store them to
+//                         tensor-memory A stages with tcgen05.st (a_full);
+//                         without split x they also fill B.
+// Tensor memory: four A stages of 32 * P columns at the top, D buffers of 32
+// (up to 32 rows of x) or 64 columns below them.  Consumer barriers count
+// warps (one elected arrival each), and waits sleep in try_wait rather than
+// spin.  When the row tiles alone do not fill the GPU, a thread-block cluster
+// of ks CTAs splits K on slot boundaries; each CTA leaves its partial y in
+// shared memory and, after a cluster barrier, CTA r sums columns r*mpad/ks ..
 // (r+1)*mpad/ks of all ks partials in rank order through distributed shared
-// memory (deterministic, no atomics).  Tiles of x beyond the first 64 rows
-// are gridDim.y.  Every wait is bounded; a timeout sets the device error word.
+// memory (deterministic, no atomics).  More than 64 rows of x take
+// qmm_mma_wide.cuh.  Every wait is bounded; a timeout sets the device error
+// word.
 #pragma once
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
