@@ -266,7 +266,6 @@ class DeviceWorkload:
             self.launches_per_step = 2 if self.planes else 1
             return
         n = 0
-        tc_min = lean.lean_tensor_core_min_m()
         for i, lin in enumerate(self.lins):
             x = self.x.data_ptr() + 4 * self.x_off[i]
             y = self.y.data_ptr() + 4 * self.y_off[i]
@@ -275,8 +274,8 @@ class DeviceWorkload:
             if lin.M == 1:
                 planes = lin.fmt != syn.Q6_K and lean.lean_packed_bytes(lin.fmt, lin.N, lin.K) >= 32 << 20
                 n += 2 if planes else 1
-            elif lin.M < tc_min:
-                n += (lin.M + 15) // 16       # CUDA-core kernel per 16 rows of x
+            elif lin.M < lean.lean_tensor_core_min_m(lin.fmt):
+                n += 1                        # CUDA-core kernel
             else:
                 n += 2                        # x split + tensor-core product
         self.launches_per_step = n
@@ -658,7 +657,7 @@ def time_linear(lin, device, l2, stream, reps=20):
     torch.cuda.synchronize()
     t = ev0.elapsed_time(ev1) / reps / dw.copies * 1e-3
     gbs = lin.algorithmic_bytes / t / 1e9
-    path = linear_path(lin, dw.lean.lean_tensor_core_min_m())
+    path = linear_path(lin, dw.lean.lean_tensor_core_min_m(lin.fmt))
     r = {"linear": lin.name, "fmt": syn.FORMAT_NAMES[lin.fmt], "N": lin.N, "K": lin.K,
          "M": lin.M, "path": path, "us": round(t * 1e6, 3), "GB/s": round(gbs, 1),
          "frac": round(gbs / peak, 4), "useful_TFLOP/s": round(lin.flops / t / 1e12, 3),

@@ -12,10 +12,13 @@ namespace lean {
 
 constexpr int kMaxBatch = LEAN_MAX_BATCH;  // problems per batched launch
 constexpr int kMaxStreamCtas = 512;        // CTAs of one streaming launch, at most
-#ifndef LEAN_MMA_MIN_M
-#define LEAN_MMA_MIN_M 16
-#endif
-constexpr int64_t kMmaMinM = LEAN_MMA_MIN_M;  // rows of x from which the tensor cores take over
+// Rows of x from which the tensor cores take over, measured: the CUDA-core
+// kernels cost about M times their one-row work (their M = 9..15 variant twice
+// the M = 5..8 one), the tensor-core kernel is flat up to 64 rows (x rows are
+// padded to 16).  At 9 rows it is ahead for every format and shape measured
+// (1.2-2.5x); Q6_K, whose 6-bit fields are dear to decode on the CUDA cores,
+// already from 5.
+inline int64_t mma_min_m(int fmt) { return fmt == LEAN_Q6_K ? 5 : 9; }
 
 struct HostProb {
     const uint8_t *W;

@@ -164,16 +164,16 @@ lean_status launch_simt(const Geom &g, const uint8_t *W, const float *x, float *
 template <int FMT>
 lean_status simt_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
                      unsigned flags, cudaStream_t stream) {
-    // M rows of x in tiles of at most 16; each tile re-streams the weights
-    for (int64_t m0 = 0; m0 < M; m0 += 16) {
-        const int mt = (int)std::min<int64_t>(16, M - m0);
+    // M rows of x in tiles of at most 8 (the library sends fewer rows than
+    // the tensor-core switch, at most 8); each tile re-streams the weights
+    for (int64_t m0 = 0; m0 < M; m0 += 8) {
+        const int mt = (int)std::min<int64_t>(8, M - m0);
         const float *xt = x + m0 * g.K;
         float *yt = y + m0 * g.N;
         lean_status s;
         if (mt <= 2) s = launch_simt<FMT, 2>(g, W, xt, yt, mt, flags, stream);
         else if (mt <= 4) s = launch_simt<FMT, 4>(g, W, xt, yt, mt, flags, stream);
-        else if (mt <= 8) s = launch_simt<FMT, 8>(g, W, xt, yt, mt, flags, stream);
-        else s = launch_simt<FMT, 16>(g, W, xt, yt, mt, flags, stream);
+        else s = launch_simt<FMT, 8>(g, W, xt, yt, mt, flags, stream);
         if (s != LEAN_OK) return s;
     }
     return LEAN_OK;
@@ -537,8 +537,9 @@ lean_status gemv_fmt(const HostProb *ph, int n, unsigned flags, cudaStream_t str
     return launch_gemv<FMT, kMaxBatch, 1, false>(ph, n, 1, flags, true, stream, done);
 }
 
-// M = 2..16 rows of x on the same kernel (several waves allowed) when a row
-// fits a cluster; *done = false leaves the call to the CUDA-core kernel.
+// M = 2..8 rows of x on the same kernel (several waves allowed; the library
+// sends it fewer rows than the tensor-core switch) when a row fits a cluster;
+// *done = false leaves the call to the row-tiled CUDA-core kernel.
 template <int FMT>
 lean_status gemv_small_m_fmt(const HostProb &hp, int M, unsigned flags, cudaStream_t stream,
                              bool *done) {
@@ -549,7 +550,8 @@ lean_status gemv_small_m_fmt(const HostProb &hp, int M, unsigned flags, cudaStre
         return LEAN_OK;
     }
     if (M <= 8) return launch_gemv<FMT, 1, 8, false>(&hp, 1, M, flags, false, stream, done);
-    return launch_gemv<FMT, 1, 16, false>(&hp, 1, M, flags, false, stream, done);
+    *done = false;
+    return LEAN_OK;
 }
 
 // -------------------------------------------------------------- stream path ---

@@ -163,7 +163,7 @@ lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_de
         HostProb hp = {W, x_dev, y_dev, g};
         return dispatch_m1(fmt, &hp, 1, flags, workspace, workspace_bytes, s);
     }
-    if (M >= kMmaMinM) {
+    if (M >= mma_min_m(fmt)) {
         unsigned *err = error_word();
         if (!err) return LEAN_ERR_CUDA;
         void *ws = workspace;
@@ -176,7 +176,7 @@ lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_de
         }
         return LEAN_ERR_FORMAT;
     }
-    {  // 2..15 rows: the one-wave kernel when a row fits a cluster of it
+    {  // fewer rows: the one-wave kernel when a row fits a cluster of it
         HostProb hp = {W, x_dev, y_dev, g};
         bool done = false;
         lean_status st2 = LEAN_OK;
@@ -209,12 +209,12 @@ lean_status lean_qmatmul(int fmt, const void *W_packed_dev, const float *x_dev, 
     return lean_qmatmul_ws(fmt, W_packed_dev, x_dev, y_dev, N, K, M, 0u, nullptr, 0, stream);
 }
 
-int lean_tensor_core_min_m(void) { return (int)kMmaMinM; }
+int lean_tensor_core_min_m(int fmt) { return lean_block_elems(fmt) > 0 ? (int)mma_min_m(fmt) : -1; }
 
 int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M) {
     Geom g;
     if (M <= 0 || !make_geom(fmt, N, K, &g)) return -1;
-    if (M >= kMmaMinM) return mma_xs_bytes(M, K);
+    if (M >= mma_min_m(fmt)) return mma_xs_bytes(M, K);
     if (M > 1) return 0;
     return workspace_layout(g.groups, xq_bytes(fmt, K)).total;
 }

@@ -38,7 +38,7 @@ constexpr int kGemvMaxCluster = 8;
 
 // Blocks a lane holds in registers at most (four 16-byte vectors per block of
 // the int8 formats: Q8_0 2, I8_B64 4; Q6_K 13 vectors), for MT rows of x: with
-// 8 or 16 rows fewer, so that the CTA's x slice stays within 32 KB.
+// 8 rows fewer, so that the CTA's x slice stays within 32 KB.
 template <int FMT> struct GemvCfg;
 template <> struct GemvCfg<Q4_0> { static constexpr int NB = 8; };
 template <> struct GemvCfg<Q8_0> { static constexpr int NB = 4; };

@@ -1,5 +1,5 @@
-// qmm_simt.cuh -- CUDA-core product for 2..16 activation rows, and the
-// dequantisation kernel.
+// qmm_simt.cuh -- CUDA-core product for a few activation rows (up to 8 per
+// launch), and the dequantisation kernel.
 //
 // One lane owns one row of a 32-row group and walks its blocks with 16-byte
 // loads (512 contiguous bytes per warp); each block is unpacked once into

@@ -43,7 +43,7 @@ SIGNATURES = {
     "lean_qmatmul": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "lean_qmatmul_ex": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp]),
     "lean_qmatmul_workspace_bytes": (_i64, [_int, _i64, _i64, _i64]),
-    "lean_tensor_core_min_m": (_int, []),
+    "lean_tensor_core_min_m": (_int, [_int]),
     "lean_qmatmul_ws": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp, _i64,
                                _vp]),
     "lean_batch_workspace_bytes": (_i64, [_int, _int, _vp]),
@@ -218,9 +218,9 @@ def lean_qmatmul_workspace_bytes(fmt: int, N: int, K: int, M: int) -> int:
     return _lib.lean_qmatmul_workspace_bytes(fmt, N, K, M)
 
 
-def lean_tensor_core_min_m() -> int:
-    """Rows of x from which the product runs on the tensor cores."""
-    return _lib.lean_tensor_core_min_m()
+def lean_tensor_core_min_m(fmt: int) -> int:
+    """Rows of x from which the product of format fmt runs on the tensor cores."""
+    return _lib.lean_tensor_core_min_m(fmt)
 
 
 def lean_qmatmul_ws(fmt: int, W_packed_dev, x_dev, y_dev, N: int, K: int, M: int,

@@ -170,10 +170,11 @@ lean_status lean_embed_rows(int fmt, const void *W_packed_dev, const int32_t *id
  *   stream        cudaStream_t as void*
  * M = 1 is the decode GEMV: a product whose row groups fit the GPU in one
  * wave runs on a kernel that loads all of its weights first and reduces on
- * chip, a larger one streams its weights through a TMA ring.  M = 2..15 runs
- * on the CUDA cores with each decoded weight reused M times (when a row fits
- * one wave; else a row-tiled kernel).  M >= 16 (lean_tensor_core_min_m())
- * runs on the tcgen05 tensor cores, every format: up to 64 rows of x, the
+ * chip, a larger one streams its weights through a TMA ring.  From M = 2 up to
+ * lean_tensor_core_min_m(fmt) - 1 rows (8; Q6_K 4) the product runs on the
+ * CUDA cores with each decoded weight reused M times (when a row fits one
+ * wave; else a row-tiled kernel).  From lean_tensor_core_min_m(fmt) rows on
+ * it runs on the tcgen05 tensor cores, every format: up to 64 rows of x, the
  * integer codes times x = x_hi + x_lo (bf16) with each block scale applied
  * after the MMAs in fp32; more rows, w = w_hi + w_lo times x_hi + x_lo (three
  * MMAs per K step).  Accuracy: |y - y_exact| <= 1e-4 * sum_k |w x| + 1e-6
@@ -245,14 +246,17 @@ lean_status lean_qmatmul_swiglu(int fmt, const void *W_gate_dev, const void *W_u
                                 const float *x_dev, float *h_dev, int64_t N, int64_t K,
                                 unsigned flags, void *stream);
 
-/* Rows of x from which lean_qmatmul uses the tensor cores (16).  Pages:
- * "oxinfer" crate page, Platforms and accelerators (the GPU takes matmuls of
- * t >= 16 tokens). */
-int lean_tensor_core_min_m(void);
+/* Rows of x from which lean_qmatmul uses the tensor cores for format fmt: 9
+ * (Q4_0, Q8_0, INT8-B64) or 5 (Q6_K); -1 for an unknown format.  The pages
+ * hand matmuls of 16 or more tokens from the CPU to the GPU ("oxinfer" crate
+ * page, Platforms and accelerators); on the GPU the switch from the CUDA-core
+ * kernels to the tensor-core one is set where the measured times cross. */
+int lean_tensor_core_min_m(int fmt);
 
 /* Bytes of device workspace that lean_qmatmul_ws uses for this shape (0 when
- * it uses none: M = 2..15), or -1 on a bad fmt or shape.  M = 1: stream-K
- * partial sums and counters.  M >= 16: x split into bf16 hi / lo operand
+ * it uses none: 2 <= M < lean_tensor_core_min_m(fmt)), or -1 on a bad fmt or
+ * shape.  M = 1: stream-K partial sums and counters.  From
+ * lean_tensor_core_min_m(fmt) rows on: x split into bf16 hi / lo operand
  * tiles, 4 bytes per element of x with M padded to 16 and K to 64.  (No
  * counterpart on the pages: scratch of this library's kernels.) */
 int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);
@@ -283,12 +287,12 @@ int64_t lean_qmatmul_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);
  *                    which holds an Inf or NaN, is marked and takes the exact
  *                    fp32 dot instead: every product w*x errs by at most
  *                    2^-14 * |w*x| before the fp32 sums, whatever x is.
- *                    M >= 16: any contents; a first kernel writes x there as
- *                    bf16 hi / lo operand tiles, once for all CTAs, which the
- *                    product then copies with TMA (the fast path for large M).
+ *                    M >= lean_tensor_core_min_m(fmt): any contents; a first
+ *                    kernel writes x there as bf16 hi / lo operand tiles, once
+ *                    for all CTAs, which the product then copies with TMA.
  *   workspace_bytes  its size (LEAN_ERR_SHAPE if too small).
  * Calls that may run at the same time on the GPU must not share a workspace.
- * The workspace is ignored for M = 2..15. */
+ * The workspace is ignored for 2 <= M < lean_tensor_core_min_m(fmt). */
 lean_status lean_qmatmul_ws(int fmt, const void *W_packed_dev, const float *x_dev,
                             float *y_dev, int64_t N, int64_t K, int64_t M,
                             unsigned flags, void *workspace, int64_t workspace_bytes,

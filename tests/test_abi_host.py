@@ -57,12 +57,16 @@ def test_sizes(lean):
 
 
 def test_workspace_sizes(lean):
-    """M = 1: stream-K scratch; 2..15 rows: none; 16 rows and up: x split
-    into bf16 hi + lo (4 bytes per element) over rows padded to 16 within each
-    256-row tile and K padded to 64."""
+    """M = 1: stream-K scratch; fewer rows than the tensor-core switch (9,
+    Q6_K 5): none; from it on: x split into bf16 hi + lo (4 bytes per element)
+    over rows padded to 16 within each 256-row tile and K padded to 64."""
     assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 1) > 0
-    assert lean.lean_tensor_core_min_m() == 16
-    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 15) == 0
+    assert [lean.lean_tensor_core_min_m(f) for f in range(4)] == [9, 9, 9, 5]
+    assert lean.lean_tensor_core_min_m(7) == -1
+    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 8) == 0
+    assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 9) == 16 * 960 * 4
+    assert lean.lean_qmatmul_workspace_bytes(3, 960, 1024, 4) == 0
+    assert lean.lean_qmatmul_workspace_bytes(3, 960, 1024, 5) == 16 * 1024 * 4
     assert lean.lean_qmatmul_workspace_bytes(0, 960, 960, 16) == 16 * 960 * 4
     assert lean.lean_qmatmul_workspace_bytes(0, 2048, 2048, 256) == 256 * 2048 * 4
     assert lean.lean_qmatmul_workspace_bytes(0, 2048, 2048, 32) == 32 * 2048 * 4

@@ -77,7 +77,7 @@ def test_m1_paths(lean, fmt, N):
 
 
 @pytest.mark.parametrize("fmt", FMTS, ids=IDS)
-@pytest.mark.parametrize("M", [2, 5, 15])
+@pytest.mark.parametrize("M", [2, 5, 8, 15])
 def test_small_m_paths(lean, fmt, M):
     for N, nb in ((1, 1), (33, 3), (100, 9)):
         product(lean, fmt, N, ks(fmt, nb), M)

@@ -1,12 +1,12 @@
-"""GPU parity of the tensor-core products (16 or more rows of x) against the
-fp64 oracle: up to 64 rows, integer codes times split-bf16 x with the block
+"""GPU parity of the tensor-core products (from lean_tensor_core_min_m(fmt)
+rows of x: 9, Q6_K 5) against the fp64 oracle: up to 64 rows, integer codes times split-bf16 x with the block
 scales applied per group after the MMAs; more rows, split-bf16 weights times
 split-bf16 x in 256-row tiles of x.
 
 Covers ragged row tiles (N not a multiple of 128), K tails (K not a multiple
 of 64), K split over a thread-block cluster (few row tiles, long K), x tiles
 with a ragged last one (both kernels), the switch-over from the CUDA-core
-path at 16 rows, bit-exact one-hot products for Q4_0 (exact in both),
+path (both sides of it, and 15 / 16 rows), bit-exact one-hot products for Q4_0 (exact in both),
 determinism, writes confined to y, and the device error word left clear --
 each both with a caller workspace (x split once by its own kernel) and
 without one (each CTA splits its x).
@@ -63,14 +63,18 @@ def test_mma_parity(lean, fmt, N, k256, M):
     assert lean.lean_device_error(0) == 0
 
 
-@pytest.mark.parametrize("M", [15, 16])
-def test_switch_over_agrees(lean, M):
-    """Both sides of the switch from CUDA cores to tensor cores meet the bar."""
-    fmt, N, K = syn.Q4_0, 384, 2048
-    W, x = syn.make_problem(fmt, N, K, M, seed=(41, M))
-    y = run_gpu(fmt, W, x, N, K)
-    y_ref, bound = oracle.qmatmul(fmt, W, x, N, K, threads=8)
-    check_close(y, y_ref, bound, "M=%d" % M)
+@pytest.mark.parametrize("fmt", FMTS, ids=IDS)
+def test_switch_over_agrees(lean, fmt):
+    """Both sides of the switch from CUDA cores to tensor cores meet the bar,
+    and so do 15 and 16 rows (one padded x tile on the tensor cores)."""
+    m0 = lean.lean_tensor_core_min_m(fmt)
+    assert m0 == (5 if fmt == syn.Q6_K else 9)
+    N, K = 384, 2048
+    for M in sorted({m0 - 1, m0, 15, 16}):
+        W, x = syn.make_problem(fmt, N, K, M, seed=(41, fmt, M))
+        y = run_gpu(fmt, W, x, N, K)
+        y_ref, bound = oracle.qmatmul(fmt, W, x, N, K, threads=8)
+        check_close(y, y_ref, bound, "%s M=%d" % (syn.FORMAT_NAMES[fmt], M))
 
 
 def test_mma_one_hot_bit_exact_q4_0(lean):
