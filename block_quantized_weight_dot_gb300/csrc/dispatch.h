@@ -65,7 +65,7 @@ lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, i
 // M = 1 on the one-wave kernel; *done = false when the problems do not fit it
 template <int FMT>
 lean_status gemv_fmt(const HostProb *ph, int n, unsigned flags, cudaStream_t stream, bool *done);
-// M = 2..16 on the one-wave kernel; *done = false when a row does not fit it
+// M = 2..8 on the one-wave kernel; *done = false when a row does not fit it
 template <int FMT>
 lean_status gemv_small_m_fmt(const HostProb &hp, int M, unsigned flags, cudaStream_t stream,
                              bool *done);

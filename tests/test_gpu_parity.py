@@ -59,7 +59,8 @@ def test_one_hot_bit_exact(lean, fmt):
 # ---- random problems: tolerance -------------------------------------------------
 
 SHAPES = [(1, 1, 1), (32, 1, 1), (33, 2, 1), (100, 9, 1), (960, 30, 1), (65, 43, 1),
-          (130, 7, 2), (50, 9, 3), (77, 12, 4), (64, 10, 7), (96, 17, 16), (40, 6, 17)]
+          (130, 7, 2), (50, 9, 3), (77, 12, 4), (64, 10, 7), (72, 11, 8), (48, 5, 9),
+          (96, 17, 16), (40, 6, 17)]
 
 
 @pytest.mark.parametrize("fmt", FMTS, ids=IDS)
