@@ -45,7 +45,9 @@
 //                         warp, two warps per lane quarter), free the buffer
 //                         (d_empty) and add d * D_g into fp32 registers; the
 //                         scale comes from the raw slot, which these warps
-//                         release too;
+//                         release too.  Up to 32 rows of x one set of four
+//                         warps covers the columns, so the two sets take
+//                         alternate groups and add their sums at the end;
 //   warps 14-17           per two 64-wide K blocks ("stages"), turn the codes
 //                         of one row each into bf16 and store them to
 //                         tensor-memory A stages with tcgen05.st (a_full);
@@ -548,6 +550,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
     const int NI = nD % 4 == 0 && nD >= 8 ? 4 : 2;   // issuers
     const int KD = nD / NI;                          // buffers per issuer
     const int64_t chunks = a.K / 32;  // 32-element chunks of a row
+    // Up to 32 rows of x the columns fit one set of four epilogue warps: the
+    // two sets then take alternate scale groups (each D buffer read by one
+    // set) and add their sums at the end.
+    const bool esplit = mpad <= 32;
 
     // Consumer barriers count warps: each warp synchronises and one lane
     // arrives (an arrival by every thread serialises hundreds of atomic
@@ -564,7 +570,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
         }
         for (int b = 0; b < nD; ++b) {
             mbar_init(&d_full[b], 1);
-            mbar_init(&d_empty[b], kMmaEpiThreads / 32);
+            mbar_init(&d_empty[b], kMmaEpiThreads / 32 / (esplit ? 2 : 1));
         }
         mbar_init(done, NI);
         *abort_s = 0;
@@ -700,7 +706,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
         const int row = 32 * (warp & 3) + lane;
         const int q = warp & 3;
         const bool row_live = n0 / kRowsPerGroup + q < a.groups;
-        const int ncol = min(32, mpad - c0);  // 32, 16 or none
+        const int eset = c0 / 32;                        // this warp's set of four
+        const int cl0 = esplit ? 0 : c0;                 // its first column
+        const int ncol = min(32, mpad - cl0);            // 32 or 16
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         // this row's scale vector in raw slot 0
         const uint8_t *sv0 = rawring + q * RAWG + (row % kRowsPerGroup) * kVec + MmaFmt<FMT>::QV * kVecBytes;
@@ -725,6 +733,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
                             ++ue;
                         }
                     }
+                    // split sets: the other set's group (its buffer is tracked above)
+                    if (esplit && ((j * GPS + h) & 1) != eset) continue;
                     // first 32-element chunk of the group in the row, and its scale
                     const int64_t c = 2 * (int64_t)(kb0 + j) + h;
                     const float d = row_live && c < chunks ? h2f(sv[scale_slot<FMT>(c)]) : 0.f;
@@ -734,7 +744,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
                     }
                     tc_fence_after();
                     uint32_t rr[32];
-                    const uint32_t td = tmem + lane_base + dstride * b + (uint32_t)c0;
+                    const uint32_t td = tmem + lane_base + dstride * b + (uint32_t)cl0;
                     if (ncol == 32) tmem_ld32(td, rr);
                     else if (ncol == 16) tmem_ld16(td, rr);
                     tmem_wait_ld();
@@ -877,6 +887,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qmm_mma_kernel(const MmaArgs a
         for (int i = 0; i < 32; ++i) acc[i] = 0.f;
     }
     tc_fence_after();
+    if (esplit) {
+        // the second set's sums join the first set's (first + second), through
+        // the raw ring, which nothing reads any more
+        float *S = reinterpret_cast<float *>(rawring);
+        const int row = 32 * (warp & 3) + lane;
+        if (epi && c0 == 32) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) S[i * kMmaRows + row] = acc[i];
+        }
+        __syncthreads();
+        if (epi && c0 == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] += S[i * kMmaRows + row];
+        }
+    }
     pdl_wait();  // y is written below
     const int64_t nq = n0 + 32 * (warp & 3) + lane;
     if (a.ks == 1) {
