@@ -38,6 +38,8 @@ SHAPES = [
     (130, 3, 33),     # ragged row tile, odd M
     (1000, 4, 64),    # several tiles
     (96, 32, 48),     # one tile, long K: K split over a cluster
+    (96, 32, 20),     # the same with the epilogue's warp sets on alternate groups
+    (160, 24, 9),     # the fewest rows of the tensor-core path, K split
     (300, 8, 256),    # a full 256-row tile of x
     (200, 2, 257),    # two tiles of x, the last with one row
     (64, 3, 300),     # rows of x ragged in the second tile
