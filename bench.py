@@ -612,11 +612,13 @@ def mma_issued_flops(lin):
     """bf16 MMA work the tensor-core kernels issue for one product, for every
     128-row weight tile and K padded to 64.  Up to 64 rows of x: the integer
     codes times x_hi and x_lo (two MMAs per 16-wide K step; Q6_K's codes in two
-    parts, three), x rows padded to 16.  More rows: split weights times split
-    x (three MMAs per step) in 256-row tiles of x, each padded to 16."""
+    parts, three), x rows padded to 16.  More rows (Q6_K and Q8_0: more than
+    32): split weights times split x (three MMAs per step) in 256-row tiles of
+    x, each padded to 16."""
     kp = -(-lin.K // 64) * 64
     tiles = -(-lin.N // 128)
-    if lin.M <= 64:
+    wide_from = 32 if lin.fmt in (syn.Q6_K, syn.Q8_0) else 64
+    if lin.M <= wide_from:
         per_step = 3 if lin.fmt == syn.Q6_K else 2
         mp = -(-lin.M // 16) * 16
     else:
@@ -668,8 +670,8 @@ def time_linear(lin, device, l2, stream, reps=20):
                             "frac_of_bf16_peak": round(issued / bf16_peak, 4),
                             "peak": bf16_peak, "peak_source": bf16_kind,
                             "basis": "bf16 MMA work the kernels issue (per 16-wide K step 2 MMAs "
-                                     "up to 64 rows of x, Q6_K 3; 3 above 64 rows; x rows padded "
-                                     "to 16, K to 64) over CUDA-event time"}
+                                     "up to 64 rows of x (Q6_K 3; Q6_K and Q8_0 up to 32); 3 "
+                                     "above; x rows padded to 16, K to 64) over CUDA-event time"}
     del dw, g
     torch.cuda.empty_cache()
     return r

@@ -351,8 +351,13 @@ template <int FMT>
 lean_status mma_fmt(const Geom &g, const uint8_t *W, const float *x, float *y, int64_t M,
                     unsigned flags, void *ws, int64_t ws_bytes, unsigned *err,
                     cudaStream_t stream) {
-    // more than one 64-row tile of x: one weight conversion per 256 rows
-    if (M > kMmaMaxN) return mma_wide_fmt<FMT>(g, W, x, y, M, flags, ws, ws_bytes, err, stream);
+    // more than one 64-row tile of x: one weight conversion per 256 rows.
+    // Q6_K and Q8_0 take it from 33 rows already: there the full epilogue of
+    // the integer-code kernel (32 columns per warp and group) costs more than
+    // the split weights' third MMA (measured: Q6_K 18992 x 2048, 48 rows,
+    // 32.0 -> 29.7 us; Q4_0 and INT8-B64 at 11008 x 2048 and 2048 x 5632 lose).
+    constexpr int64_t wide_from = (FMT == Q6_K || FMT == Q8_0) ? 32 : kMmaMaxN;
+    if (M > wide_from) return mma_wide_fmt<FMT>(g, W, x, y, M, flags, ws, ws_bytes, err, stream);
     static std::atomic<uint64_t> smem_done{0}, smem_done_x{0};
     const int64_t tiles = (g.N + kMmaRows - 1) / kMmaRows;
     const int nkb = (int)((g.K + kMmaKB - 1) / kMmaKB);

@@ -174,10 +174,10 @@ lean_status lean_embed_rows(int fmt, const void *W_packed_dev, const int32_t *id
  * lean_tensor_core_min_m(fmt) - 1 rows (8; Q6_K 4) the product runs on the
  * CUDA cores with each decoded weight reused M times (when a row fits one
  * wave; else a row-tiled kernel).  From lean_tensor_core_min_m(fmt) rows on
- * it runs on the tcgen05 tensor cores, every format: up to 64 rows of x, the
- * integer codes times x = x_hi + x_lo (bf16) with each block scale applied
- * after the MMAs in fp32; more rows, w = w_hi + w_lo times x_hi + x_lo (three
- * MMAs per K step).  Accuracy: |y - y_exact| <= 1e-4 * sum_k |w x| + 1e-6
+ * it runs on the tcgen05 tensor cores, every format: up to 64 rows of x (Q6_K
+ * and Q8_0: 32), the integer codes times x = x_hi + x_lo (bf16) with each
+ * block scale applied after the MMAs in fp32; more rows, w = w_hi + w_lo
+ * times x_hi + x_lo (three MMAs per K step).  Accuracy: |y - y_exact| <= 1e-4 * sum_k |w x| + 1e-6
  * per element.  Nothing is allocated: without a workspace (lean_qmatmul_ws)
  * the tensor-core path splits x inside each CTA. */
 lean_status lean_qmatmul(int fmt, const void *W_packed_dev, const float *x_dev,
